@@ -1,0 +1,180 @@
+/*
+ * mxq.h -- C ABI of the GB300 (sm_103a) MX quantized-training library.
+ *
+ * The library implements the hot path of microscaling (MX) quantized
+ * training: block-of-32 quantization of bf16 tensors to E4M3 (MXFP8) or
+ * E2M1 (MXFP4) element codes with one E8M0 shared exponent per block, a
+ * fixed 32-point Hadamard rotation fused into the quantizer, and the
+ * block-scaled GEMM that consumes the codes for the forward, dgrad and Wgrad
+ * products.
+ *
+ * Sources of the operations (cited per entry point below):
+ *  [AMD-FP4]  "AMD顛覆行業認知！終于攻克FP4大模型訓練致命難題" (hzrcw.cc):
+ *             §02 microscaling (each small block has its own dynamic
+ *             exponent), the deterministic Hadamard rotation on the Wgrad
+ *             path, the per-path FP4 study (forward, activation gradient,
+ *             weight gradient); §03 native FP4 GEMMs on the GPU.
+ *  [MINDSPEED] "MindSpeed LLM FSDP2量化特性：低比特大模型训练完全指南",
+ *             第 1 步 (recipe dynamic_MX-1-1-32_E4M3_E4M3_E4M3): MX
+ *             granularity, block size 32, E4M3 for inputs, weights and
+ *             gradients.
+ *  [LUMEN]    "Lumen：AMD原生大模型量化训练框架的技术突破与实践", §1: FP8
+ *             E4M3 / MXFP8 / FP4 formats.
+ *  Bit layouts and rounding (none are printed on those pages) follow the
+ *  OCP Microscaling Formats (MX) v1.0 and OCP FP8 specifications.
+ *
+ * Conventions shared by every call
+ *  - All pointers named x, codes, scales, A, B, C, out, workspace are DEVICE
+ *    pointers owned by the caller; the library never frees or keeps them.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call only enqueues work on that stream and returns;
+ *    argument errors are reported synchronously, device-side errors (a wait
+ *    that timed out) by mxq_check().
+ *  - Tensors are row-major.  A [rows, cols] bf16 tensor has row stride cols.
+ *  - E4M3 codes take one byte per element.  E2M1 codes take half a byte:
+ *    two per byte along the blocked axis, the even element in the low nibble.
+ *  - E8M0 scale bytes: value 2^(s-127); 0xFF marks a block that held a NaN
+ *    or an infinity (its codes are then all zero).  An all-zero block has
+ *    scale 0x00.
+ *  - Shared exponent e = floor(log2(amax)) - emax_elem (emax_elem = 8 for
+ *    E4M3, 2 for E2M1), clamped to [-127, 127]; elements x * 2^-e are
+ *    rounded to nearest, ties to even, saturating at 448 (E4M3) or 6 (E2M1);
+ *    a negative value that rounds to zero keeps its sign.
+ *  - Pointers to bf16 data and to codes must be 16-byte aligned; scales may
+ *    have any alignment.
+ *  - No call allocates device memory.
+ */
+#ifndef MXQ_H
+#define MXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MXQ_OK = 0,
+  MXQ_ERR_ARG = 1,          /* a size, enum or pointer argument is invalid   */
+  MXQ_ERR_ALIGN = 2,        /* a pointer or a dimension breaks an alignment rule */
+  MXQ_ERR_UNSUPPORTED = 3,  /* valid request the library does not implement   */
+  MXQ_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed               */
+  MXQ_ERR_TIMEOUT = 5,      /* a device-side wait gave up (see mxq_check)      */
+  MXQ_ERR_WORKSPACE = 6     /* workspace too small                             */
+} mxq_status;
+
+typedef enum { MXQ_E4M3 = 0, MXQ_E2M1 = 1 } mxq_fmt;
+
+typedef enum {
+  /* blocks of 32 run along cols; codes [rows][cols] (E2M1: [rows][cols/2]),
+     scales [rows][cols/32] */
+  MXQ_ROWWISE = 0,
+  /* blocks of 32 run along rows; output stored transposed: codes
+     [cols][rows] (E2M1: [cols][rows/2]), scales [cols][rows/32].  Row c of
+     the output holds input column c in row order (the Wgrad operand). */
+  MXQ_COLWISE_T = 1
+} mxq_layout;
+
+typedef enum { MXQ_OUT_F32 = 0, MXQ_OUT_BF16 = 1 } mxq_out;
+
+/* Library version, (major << 16) | minor. */
+int mxq_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* mxq_status_str(int status);
+
+/*
+ * MX quantization of a bf16 tensor x [rows][cols].
+ *   [AMD-FP4] §02 (per-block dynamic exponent), [MINDSPEED] 第 1 步
+ *   (block 32, E4M3).
+ * layout: MXQ_ROWWISE needs cols % 32 == 0; MXQ_COLWISE_T needs
+ *   rows % 32 == 0 and cols % 8 == 0.
+ * fmt: MXQ_E4M3 or MXQ_E2M1.  codes / scales: outputs in the layout above.
+ * rows == 0 or cols == 0 is a no-op.  Dimensions must be < 2^31.
+ */
+mxq_status mxq_quantize(const void* x, int64_t rows, int64_t cols, int layout, int fmt,
+                        void* codes, uint8_t* scales, void* stream);
+
+/*
+ * Fixed 32-point Hadamard rotation of every block along the quantization
+ * axis, then MX quantization of the rotated values.
+ *   [AMD-FP4] §02: a deterministic (fixed, not random) orthogonal rotation
+ *   applied before the MXFP4 quantization of the weight-gradient operands.
+ * The rotation is the natural-order Sylvester transform H_32/sqrt(32):
+ * radix-2 stages with half-width 1, 2, 4, 8, 16 in fp32, each add and
+ * subtract rounded to nearest (no fused operations), then one multiply by
+ * RN_fp32(2^-2.5).  The fp32 result is quantized without a bf16 rounding.
+ * Arguments and preconditions as mxq_quantize.
+ */
+mxq_status mxq_hadamard_quantize(const void* x, int64_t rows, int64_t cols, int layout, int fmt,
+                                 void* codes, uint8_t* scales, void* stream);
+
+/*
+ * One read of x [rows][cols] produces both the row-wise output (fmt_r,
+ * Hadamard if had_r != 0) and the column-wise transposed output (fmt_c,
+ * Hadamard if had_c != 0).  The forward/dgrad operand and the Wgrad operand
+ * of the same tensor ([AMD-FP4] §02) come from a single pass.
+ * Needs rows % 32 == 0, cols % 32 == 0.  Outputs as in mxq_quantize.
+ */
+mxq_status mxq_quantize_dual(const void* x, int64_t rows, int64_t cols,
+                             int fmt_r, int had_r, void* codes_r, uint8_t* scales_r,
+                             int fmt_c, int had_c, void* codes_c, uint8_t* scales_c,
+                             void* stream);
+
+/*
+ * Dequantization: out[r][c] = dec(code) * 2^(s-127), exact in fp32 (an
+ * overflow gives inf; scale 0xFF gives NaN); bf16 output is that fp32 value
+ * rounded to nearest even.  OCP MX v1.0 (value of an MX element).
+ * rows, cols, layout and fmt describe the tensor as it was quantized
+ * (codes laid out as mxq_quantize wrote them); out is always [rows][cols].
+ * out_dtype: MXQ_OUT_F32 or MXQ_OUT_BF16.
+ */
+mxq_status mxq_dequantize(const void* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                          int layout, int fmt, void* out, int out_dtype, void* stream);
+
+/*
+ * Block-scaled GEMM C[m][n] = sum_k dec(A[m][k]) * dec(B[n][k]) with fp32
+ * accumulation on the tensor cores.
+ *   [AMD-FP4] §02-§03: the forward (Y = X W^T), dgrad (dX = dY W) and Wgrad
+ *   (dW = dY^T X) products run on MX codes.
+ * A: codes [M][K] (E2M1: [M][K/2]), sA [M][K/32]; B: codes [N][K]
+ * (E2M1: [N][K/2]), sB [N][K/32] -- both "K-major", as MXQ_ROWWISE (or
+ * MXQ_COLWISE_T for the transposed operand) writes them.  Both operands use
+ * the same fmt.  C: [M][N] row-major, fp32 or bf16 (out_dtype).
+ * K % 32 == 0, M >= 1, N >= 1; N % 4 == 0 (fp32) / N % 8 == 0 (bf16).
+ * workspace: device scratch of at least mxq_gemm_workspace_size() bytes,
+ * 256-byte aligned; it receives the scales in the tensor-core layout.
+ */
+mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, int fmt,
+                    int64_t M, int64_t N, int64_t K, void* C, int out_dtype,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace mxq_gemm needs for this problem (0 on bad arguments). */
+size_t mxq_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int fmt);
+
+/*
+ * Synchronizes `stream`, then reports and clears device-side errors recorded
+ * by earlier calls on any stream (MXQ_ERR_TIMEOUT when a bounded wait inside
+ * a kernel gave up), or MXQ_ERR_CUDA when the stream reports a CUDA error.
+ */
+mxq_status mxq_check(void* stream);
+
+/*
+ * Upper bound, in nanoseconds, of every device-side wait (default 2e9).
+ * A kernel whose wait runs out records MXQ_ERR_TIMEOUT and returns early.
+ */
+void mxq_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Test hook for the failure path: launches one CTA that waits on a barrier
+ * no one completes, with the given limit, so that the bounded wait expires
+ * and records MXQ_ERR_TIMEOUT for mxq_check() to report.
+ */
+mxq_status mxq_debug_expire_wait(uint64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H */

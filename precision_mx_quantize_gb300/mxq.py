@@ -1,0 +1,207 @@
+"""ctypes binding of libmxq.so, the sm_103a MX quantized-training library.
+
+Argument marshalling only: every operation runs in the CUDA library.  torch
+is used to allocate device memory and to name the current stream.  If the
+library has not been built, every call raises -- there is no CPU fallback.
+
+Low-level functions keep the C names (``mxq_quantize`` ...) and take raw
+pointers; the tensor-level helpers follow the names of the method's
+statement: ``mx_quantize``, ``hadamard_mx_quantize``, ``mx_quantize_dual``,
+``mx_dequantize``, ``mx_gemm``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmxq.so")
+
+E4M3, E2M1 = 0, 1
+ROWWISE, COLWISE_T = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
+FMTS = {"e4m3": E4M3, "e2m1": E2M1, E4M3: E4M3, E2M1: E2M1}
+AXES = {"row": ROWWISE, "col": COLWISE_T, ROWWISE: ROWWISE, COLWISE_T: COLWISE_T}
+
+STATUS = {0: "MXQ_OK", 1: "MXQ_ERR_ARG", 2: "MXQ_ERR_ALIGN", 3: "MXQ_ERR_UNSUPPORTED",
+          4: "MXQ_ERR_CUDA", 5: "MXQ_ERR_TIMEOUT", 6: "MXQ_ERR_WORKSPACE"}
+
+# C signatures: (name, restype, argtypes)
+_I64, _P, _I, _SZ, _U64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint64
+SIGNATURES = [
+    ("mxq_version", ctypes.c_int, []),
+    ("mxq_status_str", ctypes.c_char_p, [_I]),
+    ("mxq_quantize", _I, [_P, _I64, _I64, _I, _I, _P, _P, _P]),
+    ("mxq_hadamard_quantize", _I, [_P, _I64, _I64, _I, _I, _P, _P, _P]),
+    ("mxq_quantize_dual", _I, [_P, _I64, _I64, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
+    ("mxq_dequantize", _I, [_P, _P, _I64, _I64, _I, _I, _P, _I, _P]),
+    ("mxq_gemm", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P, _SZ, _P]),
+    ("mxq_gemm_workspace_size", _SZ, [_I64, _I64, _I64, _I]),
+    ("mxq_check", _I, [_P]),
+    ("mxq_set_wait_timeout_ns", None, [_U64]),
+    ("mxq_debug_expire_wait", _I, [_U64, _P]),
+]
+
+_lib = None
+_lock = threading.Lock()
+
+
+class MXQError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"libmxq.so is not built ({LIB_PATH} missing); run "
+                        "precision_mx_quantize_gb300.build.build() first")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, res, args in SIGNATURES:
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def _stream(device=None) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ok(status: int, where: str):
+    if status != 0:
+        raise MXQError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+# ---- raw C-ABI calls (pointers and sizes) ------------------------------------
+
+def mxq_quantize(x, rows, cols, layout, fmt, codes, scales, stream):
+    return lib().mxq_quantize(x, rows, cols, layout, fmt, codes, scales, stream)
+
+
+def mxq_hadamard_quantize(x, rows, cols, layout, fmt, codes, scales, stream):
+    return lib().mxq_hadamard_quantize(x, rows, cols, layout, fmt, codes, scales, stream)
+
+
+def mxq_quantize_dual(x, rows, cols, fmt_r, had_r, codes_r, scales_r, fmt_c, had_c, codes_c,
+                      scales_c, stream):
+    return lib().mxq_quantize_dual(x, rows, cols, fmt_r, had_r, codes_r, scales_r, fmt_c, had_c,
+                                   codes_c, scales_c, stream)
+
+
+def mxq_dequantize(codes, scales, rows, cols, layout, fmt, out, out_dtype, stream):
+    return lib().mxq_dequantize(codes, scales, rows, cols, layout, fmt, out, out_dtype, stream)
+
+
+def mxq_gemm(A, sA, B, sB, fmt, M, N, K, C, out_dtype, workspace, ws_bytes, stream):
+    return lib().mxq_gemm(A, sA, B, sB, fmt, M, N, K, C, out_dtype, workspace, ws_bytes, stream)
+
+
+def mxq_gemm_workspace_size(M, N, K, fmt):
+    return lib().mxq_gemm_workspace_size(M, N, K, fmt)
+
+
+def mxq_check(stream=None):
+    return lib().mxq_check(stream)
+
+
+def check(device=None):
+    """Synchronize the current stream and raise on any recorded device error."""
+    _ok(mxq_check(_stream(device)), "mxq_check")
+
+
+def set_wait_timeout_ns(ns: int):
+    lib().mxq_set_wait_timeout_ns(int(ns))
+
+
+# ---- tensor-level helpers -----------------------------------------------------
+
+def code_shape(rows: int, cols: int, axis, fmt):
+    """(codes shape, scales shape) for a [rows, cols] tensor."""
+    ax, f = AXES[axis], FMTS[fmt]
+    r, c = (rows, cols) if ax == ROWWISE else (cols, rows)
+    return (r, c if f == E4M3 else c // 2), (r, c // 32)
+
+
+def _alloc_codes(x, axis, fmt):
+    cs, ss = code_shape(x.shape[0], x.shape[1], axis, fmt)
+    return (torch.empty(cs, dtype=torch.uint8, device=x.device),
+            torch.empty(ss, dtype=torch.uint8, device=x.device))
+
+
+def mx_quantize(x: torch.Tensor, axis="row", fmt="e4m3", out=None):
+    """MX-quantize a contiguous bf16 CUDA tensor [rows, cols]; returns (codes, scales)."""
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    codes, scales = out if out is not None else _alloc_codes(x, axis, fmt)
+    _ok(mxq_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
+                     codes.data_ptr(), scales.data_ptr(), _stream(x.device)), "mxq_quantize")
+    return codes, scales
+
+
+def hadamard_mx_quantize(x: torch.Tensor, axis="col", fmt="e2m1", out=None):
+    """Fixed 32-point Hadamard rotation of each block, then MX quantization."""
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    codes, scales = out if out is not None else _alloc_codes(x, axis, fmt)
+    _ok(mxq_hadamard_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
+                              codes.data_ptr(), scales.data_ptr(), _stream(x.device)),
+        "mxq_hadamard_quantize")
+    return codes, scales
+
+
+def mx_quantize_dual(x: torch.Tensor, fmt_r="e4m3", had_r=False, fmt_c="e2m1", had_c=True,
+                     out=None):
+    """One pass producing the row-wise and the column-wise (transposed) outputs."""
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    if out is None:
+        cr, sr = _alloc_codes(x, "row", fmt_r)
+        cc, sc = _alloc_codes(x, "col", fmt_c)
+    else:
+        cr, sr, cc, sc = out
+    _ok(mxq_quantize_dual(x.data_ptr(), x.shape[0], x.shape[1], FMTS[fmt_r], int(had_r),
+                          cr.data_ptr(), sr.data_ptr(), FMTS[fmt_c], int(had_c), cc.data_ptr(),
+                          sc.data_ptr(), _stream(x.device)), "mxq_quantize_dual")
+    return cr, sr, cc, sc
+
+
+def mx_dequantize(codes, scales, rows, cols, axis="row", fmt="e4m3", out_dtype=torch.float32,
+                  out=None):
+    """Dequantize codes written by mx_quantize back to a [rows, cols] tensor."""
+    od = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype, device=codes.device)
+    _ok(mxq_dequantize(codes.data_ptr(), scales.data_ptr(), rows, cols, AXES[axis], FMTS[fmt],
+                       out.data_ptr(), od, _stream(codes.device)), "mxq_dequantize")
+    return out
+
+
+def gemm_workspace(M, N, K, fmt, device):
+    n = mxq_gemm_workspace_size(M, N, K, FMTS[fmt])
+    return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
+
+
+def mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=torch.float32, out=None, workspace=None):
+    """C[M, N] = dec(A) @ dec(B)^T on the tensor cores (A, B K-major MX codes)."""
+    od = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    if workspace is None:
+        workspace = gemm_workspace(M, N, K, fmt, A.device)
+    _ok(mxq_gemm(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M, N, K,
+                 out.data_ptr(), od, workspace.data_ptr(), workspace.numel(),
+                 _stream(A.device)), "mxq_gemm")
+    return out

@@ -1,0 +1,35 @@
+"""Shared test helpers: locate/build the CUDA library, move data for the oracle."""
+
+import os
+
+import numpy as np
+import torch
+
+from precision_mx_quantize_gb300 import build as _build
+from precision_mx_quantize_gb300 import mxq
+
+
+def ensure_built():
+    if not os.path.exists(mxq.LIB_PATH):
+        _build.build()
+    return mxq.lib()
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+def bf16_to_f32_np(x: torch.Tensor) -> np.ndarray:
+    return x.detach().float().cpu().numpy()
+
+
+def header_symbols():
+    import re
+    here = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    names = set()
+    inc = os.path.join(here, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            names |= set(re.findall(r"\b(mxq_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)

@@ -1,0 +1,53 @@
+"""Host-side checks of the C-ABI library: it loads, exports every declared
+symbol, and rejects bad arguments before any device work."""
+
+import ctypes
+
+import pytest
+
+from precision_mx_quantize_gb300 import mxq
+from tests.libutil import ensure_built, header_symbols
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ensure_built()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_symbols()
+    assert "mxq_quantize" in names and "mxq_gemm" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    bound = {n for n, _, _ in mxq.SIGNATURES}
+    assert set(names) <= bound
+
+
+def test_version_and_status_strings(lib):
+    assert lib.mxq_version() >= 1
+    assert lib.mxq_status_str(0) == b"ok"
+    assert lib.mxq_status_str(5) == b"device-side wait timed out"
+    assert lib.mxq_status_str(99) == b"unknown status"
+
+
+def test_argument_errors_return_before_device_work(lib):
+    p = ctypes.c_void_p(16 * 1024)  # never dereferenced: every call below fails its checks
+    E4, E2, ROW, COL = mxq.E4M3, mxq.E2M1, mxq.ROWWISE, mxq.COLWISE_T
+    # empty tensors are a no-op
+    assert mxq.mxq_quantize(p, 0, 64, ROW, E4, p, p, None) == 0
+    # row-wise needs cols % 32 == 0
+    assert mxq.mxq_quantize(p, 64, 48, ROW, E4, p, p, None) == 1
+    # col-wise needs rows % 32 == 0
+    assert mxq.mxq_quantize(p, 40, 64, COL, E2, p, p, None) == 1
+    # bad enums and null pointers
+    assert mxq.mxq_quantize(p, 64, 64, 7, E4, p, p, None) == 1
+    assert mxq.mxq_quantize(p, 64, 64, ROW, 9, p, p, None) == 1
+    assert mxq.mxq_quantize(None, 64, 64, ROW, E4, p, p, None) == 1
+    # misaligned input pointer
+    assert mxq.mxq_quantize(ctypes.c_void_p(16 * 1024 + 2), 64, 64, ROW, E4, p, p, None) == 2
+    # dual needs both dims % 32
+    assert mxq.mxq_quantize_dual(p, 64, 40, E4, 0, p, p, E2, 1, p, p, None) == 1
+    # negative sizes
+    assert mxq.mxq_hadamard_quantize(p, -32, 64, ROW, E2, p, p, None) == 1
+    assert mxq.mxq_dequantize(p, p, 64, 48, ROW, E4, p, 0, None) == 1
+    assert mxq.mxq_dequantize(p, p, 64, 64, ROW, E4, p, 3, None) == 1

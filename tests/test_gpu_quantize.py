@@ -1,0 +1,196 @@
+"""Parity of the CUDA quantizers and dequantizer with the CPU oracle.
+
+Codes and scales must match bit for bit (the butterfly order and the
+rounding are fixed), on tiny shapes, ragged tiles and the full-size
+workloads, including the degenerate blocks (zeros, NaN, Inf, subnormal and
+huge maxima).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mx_oracle as O
+from precision_mx_quantize_gb300 import mxq, synth
+from tests.golden.fixtures import load_blocks
+from tests.libutil import bf16_to_f32_np, ensure_built, to_np
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["e4m3", "e2m1"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    ensure_built()
+
+
+def _x(rows, cols, seed=0, kind="act"):
+    if kind == "act":
+        return synth.activation(rows, cols, seed).cuda()
+    return synth.normal_with_outliers((rows, cols), seed).cuda()
+
+
+def _check(x, axis, fmt, had):
+    xn = bf16_to_f32_np(x)
+    if had:
+        codes, scales = mxq.hadamard_mx_quantize(x, axis, fmt)
+    else:
+        codes, scales = mxq.mx_quantize(x, axis, fmt)
+    mxq.check()
+    ec, es = O.quantize_any(xn, axis, fmt, had)
+    np.testing.assert_array_equal(to_np(scales), es)
+    np.testing.assert_array_equal(to_np(codes), ec)
+
+
+ROW_SHAPES = [(1, 32), (32, 32), (33, 64), (64, 96), (128, 128), (200, 160), (257, 416)]
+COL_SHAPES = [(32, 8), (32, 32), (64, 40), (96, 136), (160, 200), (288, 392)]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("had", [False, True])
+@pytest.mark.parametrize("shape", ROW_SHAPES)
+def test_rowwise_parity(fmt, had, shape):
+    _check(_x(*shape, seed=shape[0]), "row", fmt, had)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("had", [False, True])
+@pytest.mark.parametrize("shape", COL_SHAPES)
+def test_colwise_parity(fmt, had, shape):
+    _check(_x(*shape, seed=shape[1]), "col", fmt, had)
+
+
+@pytest.mark.parametrize("fr,hr,fc,hc", [
+    ("e4m3", False, "e2m1", True),   # activations / output gradients in the block pass
+    ("e4m3", False, "e4m3", False),  # weights
+    ("e2m1", True, "e2m1", True),    # both axes rotated, E2M1
+    ("e2m1", False, "e4m3", True),
+])
+@pytest.mark.parametrize("shape", [(32, 32), (96, 160), (160, 288), (384, 256)])
+def test_dual_parity(fr, hr, fc, hc, shape):
+    x = _x(*shape, seed=7)
+    xn = bf16_to_f32_np(x)
+    cr, sr, cc, sc = mxq.mx_quantize_dual(x, fr, hr, fc, hc)
+    mxq.check()
+    er, esr = O.quantize_any(xn, "row", fr, hr)
+    ec, esc = O.quantize_any(xn, "col", fc, hc)
+    np.testing.assert_array_equal(to_np(sr), esr)
+    np.testing.assert_array_equal(to_np(cr), er)
+    np.testing.assert_array_equal(to_np(sc), esc)
+    np.testing.assert_array_equal(to_np(cc), ec)
+
+
+def _special_tensor(rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((rows, cols)) * np.exp2(rng.integers(-30, 30, (rows, 1)))).astype(np.float32)
+    flat = x.reshape(-1)
+    n = flat.size
+    idx = rng.choice(n, size=n // 50, replace=False)
+    specials = np.array([0.0, -0.0, np.nan, np.inf, -np.inf, 3.0e38, -3.3e38, 2.0 ** -133,
+                         -(2.0 ** -130), 1e-40, 448.0, 500.0, 6.0, 7.5, -5.0], dtype=np.float32)
+    flat[idx] = specials[rng.integers(0, len(specials), size=idx.size)]
+    x[:32, :32] = 0.0                       # an all-zero block on both axes
+    x[32:64, 32:64] = -0.0
+    x[64:96, :32] = 2.0 ** -130             # subnormal maxima
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    return xb
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("had", [False, True])
+def test_special_values(fmt, had):
+    x = _special_tensor(128, 256, 3 + int(had)).cuda()
+    _check(x, "row", fmt, had)
+    _check(x, "col", fmt, had)
+
+
+@pytest.mark.parametrize("case", load_blocks(), ids=lambda c: c["name"])
+def test_hand_derived_blocks_on_gpu(case):
+    x = torch.tensor(case["x"], dtype=torch.float32).to(torch.bfloat16).reshape(1, 32).cuda()
+    codes, scales = mxq.mx_quantize(x, "row", case["fmt"])
+    mxq.check()
+    c = to_np(codes)[0]
+    if case["fmt"] == "e2m1":
+        c = O.unpack_e2m1(c)
+    assert int(to_np(scales)[0, 0]) == case["scale"]
+    assert [int(v) for v in c] == case["codes"]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("axis", ["row", "col"])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_dequantize_parity(fmt, axis, out_dtype):
+    x = _special_tensor(96, 160, 11).cuda()
+    codes, scales = mxq.mx_quantize(x, axis, fmt)
+    got = mxq.mx_dequantize(codes, scales, 96, 160, axis, fmt, out_dtype)
+    mxq.check()
+    out = "f32" if out_dtype == torch.float32 else "bf16"
+    exp = O.mx_dequantize(to_np(codes), to_np(scales), fmt, out)
+    if axis == "col":
+        exp = exp.T
+    np.testing.assert_array_equal(to_np(got.float()), exp)
+
+
+def test_dequantize_arbitrary_scales():
+    # every scale byte, including 0 (subnormal 2^-127), 254 (overflow to inf)
+    # and 255 (NaN), against every E4M3 code
+    codes = torch.arange(256, dtype=torch.uint8).repeat(256, 1).reshape(256, 256)
+    scales = torch.arange(256, dtype=torch.uint8).repeat_interleave(8).reshape(256, 8)
+    codes = codes.contiguous()
+    got = mxq.mx_dequantize(codes.cuda(), scales.cuda(), 256, 256, "row", "e4m3")
+    mxq.check()
+    exp = O.mx_dequantize(codes.numpy(), scales.numpy(), "e4m3")
+    np.testing.assert_array_equal(to_np(got), exp)
+    c2 = torch.randint(0, 256, (64, 64), dtype=torch.uint8, generator=torch.Generator().manual_seed(1))
+    s2 = torch.arange(256, dtype=torch.uint8)[torch.randperm(256, generator=torch.Generator().manual_seed(2))][:256].reshape(64, 4)
+    got2 = mxq.mx_dequantize(c2.cuda(), s2.cuda(), 64, 128, "row", "e2m1")
+    mxq.check()
+    exp2 = O.mx_dequantize(c2.numpy(), s2.numpy(), "e2m1")
+    np.testing.assert_array_equal(to_np(got2), exp2)
+
+
+def test_small_round_trip_workload():
+    # 256x1024 N(0,1) with 1% x100 outliers, E4M3 row-wise, then dequantize
+    x = synth.quantize_dequantize_small()["x"].cuda()
+    codes, scales = mxq.mx_quantize(x, "row", "e4m3")
+    back = mxq.mx_dequantize(codes, scales, 256, 1024, "row", "e4m3")
+    mxq.check()
+    ec, es = O.mx_quantize(bf16_to_f32_np(x), "row", "e4m3")
+    np.testing.assert_array_equal(to_np(codes), ec)
+    np.testing.assert_array_equal(to_np(scales), es)
+    np.testing.assert_array_equal(to_np(back), O.mx_dequantize(ec, es, "e4m3"))
+
+
+def test_full_size_dual_hadamard_e2m1():
+    # 8192x4096 activation, fused Hadamard + E2M1 along rows and columns
+    x = synth.hadamard_dual_activation()["x"].cuda()
+    cr, sr, cc, sc = mxq.mx_quantize_dual(x, "e2m1", True, "e2m1", True)
+    mxq.check()
+    xn = bf16_to_f32_np(x)
+    er, esr = O.hadamard_mx_quantize(xn, "row", "e2m1")
+    np.testing.assert_array_equal(to_np(sr), esr)
+    np.testing.assert_array_equal(to_np(cr), er)
+    del er, esr
+    ec, esc = O.hadamard_mx_quantize(xn, "col", "e2m1")
+    np.testing.assert_array_equal(to_np(sc), esc)
+    np.testing.assert_array_equal(to_np(cc), ec)
+
+
+def test_deterministic_repeat():
+    x = _x(512, 768, seed=5)
+    a = mxq.mx_quantize_dual(x, "e4m3", False, "e2m1", True)
+    b = mxq.mx_quantize_dual(x, "e4m3", False, "e2m1", True)
+    mxq.check()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+def test_bounded_wait_reports_timeout():
+    s = mxq._stream()
+    assert mxq.lib().mxq_debug_expire_wait(10_000_000, s) == 0
+    assert mxq.mxq_check(s) == 5  # MXQ_ERR_TIMEOUT
+    assert mxq.mxq_check(s) == 0  # cleared after being reported
+    # the context is still usable
+    _check(_x(64, 64), "row", "e4m3", False)
