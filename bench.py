@@ -1,0 +1,539 @@
+"""Benchmark of the MX quantized-training hot path on GB300.
+
+One step = one pass of the whole path over the linear layers of one
+Llama-3.1-8B decoder block at 8192 tokens (QKV 4096->6144, O 4096->4096,
+gate+up 4096->28672, down 14336->4096).  Per layer:
+
+  X  [T, in]   -> dual quantizer: row-wise E4M3 (forward A) + column-wise
+                  Hadamard E2M1 (Wgrad B)
+  W  [out, in] -> dual quantizer: row-wise E4M3 (forward B) + column-wise
+                  E4M3 (dgrad B, i.e. W^T)
+  dY [T, out]  -> dual quantizer: row-wise E4M3 (dgrad A) + column-wise
+                  Hadamard E2M1 (Wgrad A)
+  forward  Y  = X W^T          MXFP8 GEMM, bf16 out
+  dgrad    dX = dY W           MXFP8 GEMM, bf16 out
+  Wgrad    dW = (H dY)^T (H X) MXFP4 GEMM, fp32 out
+
+Headline value: GEMM TFLOP/s of the whole step (quantizers included in the
+time).  The JSON line also carries the quantizer GB/s and the MXFP8 / MXFP4
+GEMM TFLOP/s, each against the measured GB300 peaks.
+
+Multi-GPU: the path has no exchange step, so N ranks run N independent
+replicas (weak scaling); rank 0 prints the aggregate.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MX quant GB/s & block-scaled MXFP8/MXFP4 GEMM TFLOPS, % of GB300 roofline"
+WORKLOAD = ("llama3.1-8b decoder-block linears, T=8192: dual MX quantizers + "
+            "fwd/dgrad MXFP8 (E4M3) + wgrad Hadamard-MXFP4 (E2M1) GEMMs")
+L2_BYTES = 129 * 2 ** 20
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16": float(p["bf16_tflops"]),
+                "bf16_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# Work description (shared by the GPU arm and the CPU oracle arm)
+# ---------------------------------------------------------------------------
+
+def layer_plan(tokens):
+    from precision_mx_quantize_gb300 import synth
+    out = []
+    for i, (name, fin, fout) in enumerate(synth.LLAMA8B_LINEARS):
+        out.append(dict(name=name, fin=fin, fout=fout, T=tokens, index=i))
+    return out
+
+
+def quant_bytes(rows, cols, fr, fc):
+    """Algorithmic bytes of one dual quantizer pass: bf16 in + both code/scale outputs."""
+    n = rows * cols
+    b = 2 * n
+    for f in (fr, fc):
+        b += n if f == "e4m3" else n // 2
+        b += n // 32
+    return b
+
+
+def step_work(plan):
+    q, f8, f4 = 0, 0, 0
+    for L in plan:
+        T, fin, fout = L["T"], L["fin"], L["fout"]
+        q += quant_bytes(T, fin, "e4m3", "e2m1")
+        q += quant_bytes(fout, fin, "e4m3", "e4m3")
+        q += quant_bytes(T, fout, "e4m3", "e2m1")
+        f8 += 2 * (2 * T * fout * fin)
+        f4 += 2 * T * fout * fin
+    return q, f8, f4
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _smi_id(device):
+    """nvidia-smi -i selector (PCI bus id) of a torch CUDA device."""
+    import torch
+    p = torch.cuda.get_device_properties(device)
+    try:
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except AttributeError:
+        return str(device.index or 0)
+
+
+def build_device_state(plan, device):
+    """Device inputs, preallocated outputs and workspaces for every layer."""
+    import torch
+
+    from precision_mx_quantize_gb300 import mxq, synth
+    layers = []
+    for L in plan:
+        T, fin, fout, i = L["T"], L["fin"], L["fout"], L["index"]
+        d = synth.decoder_block_layer(fin, fout, T, i)
+        st = {"L": L, "host": d}
+        st["x"] = d["x"].to(device)
+        st["w"] = d["w"].to(device)
+        st["dy"] = d["dy"].to(device)
+
+        def codes(rows, cols, axis, fmt):
+            cs, ss = mxq.code_shape(rows, cols, axis, fmt)
+            return (torch.empty(cs, dtype=torch.uint8, device=device),
+                    torch.empty(ss, dtype=torch.uint8, device=device))
+
+        st["xq"] = (*codes(T, fin, "row", "e4m3"), *codes(T, fin, "col", "e2m1"))
+        st["wq"] = (*codes(fout, fin, "row", "e4m3"), *codes(fout, fin, "col", "e4m3"))
+        st["dyq"] = (*codes(T, fout, "row", "e4m3"), *codes(T, fout, "col", "e2m1"))
+        st["y"] = torch.empty((T, fout), dtype=torch.bfloat16, device=device)
+        st["dx"] = torch.empty((T, fin), dtype=torch.bfloat16, device=device)
+        st["dw"] = torch.empty((fout, fin), dtype=torch.float32, device=device)
+        st["ws_f"] = mxq.gemm_workspace(T, fout, fin, "e4m3", device)
+        st["ws_d"] = mxq.gemm_workspace(T, fin, fout, "e4m3", device)
+        st["ws_w"] = mxq.gemm_workspace(fout, fin, T, "e2m1", device)
+        layers.append(st)
+    return layers
+
+
+# kernels launched per layer: 3 dual quantizers, 3 GEMMs each with 2 scale
+# re-layout launches
+LAUNCHES_PER_LAYER = 3 + 3 * 3
+
+
+def run_step(layers, events=None):
+    """Enqueue one pass of the hot path on the current stream."""
+    import torch
+
+    from precision_mx_quantize_gb300 import mxq
+
+    def mark(tag):
+        if events is not None:
+            e = torch.cuda.Event(enable_timing=True)
+            e.record()
+            events.append((tag, e))
+
+    for st in layers:
+        T, fin, fout = st["L"]["T"], st["L"]["fin"], st["L"]["fout"]
+        mark("q")
+        mxq.mx_quantize_dual(st["x"], "e4m3", False, "e2m1", True, out=st["xq"])
+        mxq.mx_quantize_dual(st["w"], "e4m3", False, "e4m3", False, out=st["wq"])
+        mxq.mx_quantize_dual(st["dy"], "e4m3", False, "e2m1", True, out=st["dyq"])
+        mark("f8")
+        xr, sxr, xc, sxc = st["xq"]
+        wr, swr, wc, swc = st["wq"]
+        dr, sdr, dc, sdc = st["dyq"]
+        mxq.mx_gemm(xr, sxr, wr, swr, "e4m3", T, fout, fin, torch.bfloat16, out=st["y"],
+                    workspace=st["ws_f"])
+        mxq.mx_gemm(dr, sdr, wc, swc, "e4m3", T, fin, fout, torch.bfloat16, out=st["dx"],
+                    workspace=st["ws_d"])
+        mark("f4")
+        mxq.mx_gemm(dc, sdc, xc, sxc, "e2m1", fout, fin, T, torch.float32, out=st["dw"],
+                    workspace=st["ws_w"])
+    mark("end")
+
+
+def interval_sums(events):
+    """Milliseconds spent in each tagged interval of one recorded step."""
+    sums = {}
+    for (tag, e0), (_, e1) in zip(events[:-1], events[1:]):
+        sums[tag] = sums.get(tag, 0.0) + e0.elapsed_time(e1)
+    return sums
+
+
+def reduce_max_ms(ms_local, device=None):
+    """Slowest rank's timed-region milliseconds (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    if dist.is_initialized():
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(world, flops_per_step, steps, ms_max):
+    """Whole-job throughput: every replica's GEMM flops over the slowest rank's time."""
+    return world * flops_per_step * steps / (ms_max * 1e-3) / 1e12
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from precision_mx_quantize_gb300 import mxq
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    mxq.lib()
+    plan = layer_plan(args.tokens)
+    layers = build_device_state(plan, device)
+    qbytes, f8, f4 = step_work(plan)
+    flops = f8 + f4
+
+    for _ in range(args.warmup):
+        run_step(layers)
+    mxq.check()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, per-interval events on the launching stream
+    per_step_events = []
+    sampler = ClockSampler(_smi_id(device))
+    if dist.is_initialized():
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        ev = []
+        run_step(layers, ev)
+        per_step_events.append(ev)
+    t1.record()
+    torch.cuda.synchronize()
+    if dist.is_initialized():
+        dist.barrier()
+    clocks = sampler.stop()
+    status = mxq.mxq_check(mxq._stream())
+    if status != 0:
+        raise mxq.MXQError(status, "timed region")
+    ms_total = t0.elapsed_time(t1)
+    sums = {"q": 0.0, "f8": 0.0, "f4": 0.0}
+    for ev in per_step_events:
+        for k, v in interval_sums(ev).items():
+            sums[k] += v
+
+    # ---- end to end through the public API with host buffers
+    e2e = e2e_measure(args, layers, flops, device)
+
+    ms_max = reduce_max_ms(ms_total, device)
+    if rank != 0:
+        return None
+
+    peaks = _peaks()
+    ms_step = ms_max / args.steps
+    value = aggregate_tflops(world, flops, args.steps, ms_max)
+    q_gbs = qbytes * args.steps / (sums["q"] * 1e-3) / 1e9
+    f8_tf = f8 * args.steps / (sums["f8"] * 1e-3) / 1e12
+    f4_tf = f4 * args.steps / (sums["f4"] * 1e-3) / 1e12
+    fp8_peak = 2.0 * peaks["bf16_sustained"]   # nominal fp8:bf16 = 4.5 : 2.25
+    fp4_peak = 6.0 * peaks["bf16_sustained"]   # nominal fp4:bf16 = 13.5 : 2.25
+    traffic = _profile_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3/e2m1 codes, e8m0 scales, fp32 accumulate",
+        "data": "synthetic (seeded Student-t / normal / lognormal-scaled; no dataset or weights)",
+        "config": {
+            "workload": WORKLOAD,
+            "tokens": args.tokens,
+            "layers": [f"{L['name']} {L['fin']}->{L['fout']}" for L in plan],
+            "l2": "inputs larger than L2: each step streams ~%.1f GB of distinct tensors" %
+                  ((qbytes) / 1e9),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "breakdown": {
+            "quantizers": {"GB/s": round(q_gbs, 1), "frac_of_hbm": round(q_gbs / peaks["hbm_gbs"], 3),
+                            "ms_per_step": round(sums["q"] / args.steps, 4),
+                            "bytes_per_step": qbytes},
+            "mxfp8_gemm": {"TFLOP/s": round(f8_tf, 1), "frac_of_peak": round(f8_tf / fp8_peak, 3),
+                           "ms_per_step": round(sums["f8"] / args.steps, 4), "flop_per_step": f8},
+            "mxfp4_gemm": {"TFLOP/s": round(f4_tf, 1), "frac_of_peak": round(f4_tf / fp4_peak, 3),
+                           "ms_per_step": round(sums["f4"] / args.steps, 4), "flop_per_step": f4},
+            "peaks": {"hbm_GB/s": peaks["hbm_gbs"], "mxfp8_TFLOP/s": fp8_peak,
+                      "mxfp4_TFLOP/s": fp4_peak,
+                      "basis": f"{peaks['source']} (MEASURED_PEAKS.json): HBM copy; bf16 sustained x nominal ratio"},
+        },
+        "roofline": {
+            "kernel": "mx_gemm_kernel (MXFP8 E4M3, forward + dgrad launches)",
+            "bound": "tensor",
+            "achieved": round(f8_tf, 1),
+            "peak": fp8_peak,
+            "unit": "TFLOP/s",
+            "frac": round(f8_tf / fp8_peak, 3),
+            "traffic": traffic,
+        },
+        "e2e": e2e,
+        "gpu_launches": LAUNCHES_PER_LAYER * len(plan) * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
+    return line
+
+
+def _profile_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get("mx_gemm_kernel_e4m3_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def e2e_measure(args, layers, flops, device):
+    """Same step through the public API with pinned host inputs copied in and
+    the Wgrad outputs (the step's gradients) copied back, inside the timed region."""
+    import torch
+    host_in, host_out = [], []
+    h2d = d2h = 0
+    for st in layers:
+        hi = {k: st["host"][k].pin_memory() for k in ("x", "w", "dy")}
+        host_in.append(hi)
+        h2d += sum(t.numel() * t.element_size() for t in hi.values())
+        ho = torch.empty(st["dw"].shape, dtype=st["dw"].dtype, pin_memory=True)
+        host_out.append(ho)
+        d2h += ho.numel() * ho.element_size()
+
+    def one():
+        for st, hi, ho in zip(layers, host_in, host_out):
+            st["x"].copy_(hi["x"], non_blocking=True)
+            st["w"].copy_(hi["w"], non_blocking=True)
+            st["dy"].copy_(hi["dy"], non_blocking=True)
+        run_step(layers)
+        for st, ho in zip(layers, host_out):
+            ho.copy_(st["dw"], non_blocking=True)
+
+    steps = max(1, min(args.steps, 5))
+    one()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        one()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------
+
+def _oracle_sample_step(plan, t_s, out_s, seed=0):
+    """The step's operations on a token x feature slice of every layer, in the oracle.
+
+    Returns the GEMM flops of the sample.
+    """
+    import numpy as np
+
+    from oracle import mx_oracle as O
+    from precision_mx_quantize_gb300 import synth
+    flops = 0
+    for L in plan:
+        fin = L["fin"]
+        fout = min(out_s, L["fout"])
+        x = synth.activation(t_s, fin, 3 * L["index"]).float().numpy()
+        w = synth.weight(fout, fin, 3 * L["index"] + 1).float().numpy()
+        dy = synth.out_grad(t_s, fout, 3 * L["index"] + 2).float().numpy()
+        xr = O.mx_quantize(x, "row", "e4m3")
+        xc = O.hadamard_mx_quantize(x, "col", "e2m1")
+        wr = O.mx_quantize(w, "row", "e4m3")
+        wc = O.mx_quantize(w, "col", "e4m3")
+        dr = O.mx_quantize(dy, "row", "e4m3")
+        dc = O.hadamard_mx_quantize(dy, "col", "e2m1")
+        O.mx_gemm_f64(*xr, *wr, "e4m3")
+        O.mx_gemm_f64(*dr, *wc, "e4m3")
+        O.mx_gemm_f64(*dc, *xc, "e2m1")
+        flops += 3 * 2 * t_s * fout * fin
+        del x, w, dy, xr, xc, wr, wc, dr, dc
+        _ = np
+    return flops
+
+
+def cpu_baseline(budget_s=15.0):
+    t_s, out_s = 256, 1024
+    plan = layer_plan(8192)
+    t0 = time.perf_counter()
+    flops = _oracle_sample_step(plan, t_s, out_s)
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": (f"every layer of the block pass on {t_s} tokens x {out_s} output features "
+                       f"(full input width): 6 quantizations + 3 fp64 GEMMs per layer; "
+                       f"{dt:.1f} s, numpy (BLAS threads = cores)")}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    plan = layer_plan(args.tokens)
+    t_s, out_s = 32, 128
+    for _ in range(args.warmup):
+        _oracle_sample_step(plan, t_s, out_s)
+    times, flops = [], 0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        flops = _oracle_sample_step(plan, t_s, out_s)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    sample = (f"each step: every layer of the block pass on {t_s} tokens x {out_s} output "
+              f"features (full input width) in the CPU oracle")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "tokens": args.tokens},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=8192)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local_rank = _env_int("LOCAL_RANK", 0)
+
+    if args.impl == "reference":
+        line = reference_arm(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch.distributed as dist
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", rank=rank, world_size=world)
+    try:
+        line = gpu_arm(args, rank, world, local_rank)
+    finally:
+        if dist.is_initialized():
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,59 @@
+"""World-size-2 gloo checks of the multi-rank host logic of bench.py.
+
+The MX path has no exchange step, so N GPUs run N replicas; the only
+cross-rank work is the barrier and the max-over-ranks timing reduction that
+turn per-rank times into the whole-job number.
+"""
+
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import argparse
+
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        dist.barrier()
+        ms = bench.reduce_max_ms(10.0 + 5.0 * rank)
+        val = bench.aggregate_tflops(world, 1e12, 4, ms)
+        args = argparse.Namespace(steps=1, warmup=0, tokens=8192)
+        ref = bench.reference_arm(args, rank, world) if rank != 0 else "rank0"
+        out[rank] = (ms, val, ref)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.timeout(120)
+def test_max_over_ranks_and_aggregate():
+    world = 2
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+    for r in range(world):
+        ms, val, ref = out[r]
+        assert ms == 15.0                      # the slowest rank's time, on every rank
+        assert abs(val - 2 * 1e12 * 4 / 15e-3 / 1e12) < 1e-9
+    assert out[1][2] is None                   # only rank 0 runs the reference arm
+
+
+def test_step_work_counts():
+    import bench
+    plan = bench.layer_plan(8192)
+    q, f8, f4 = bench.step_work(plan)
+    macs = sum(L["T"] * L["fin"] * L["fout"] for L in plan)
+    assert f8 == 4 * macs and f4 == 2 * macs
+    assert bench.quant_bytes(32, 64, "e4m3", "e2m1") == 2 * 2048 + 2048 + 64 + 1024 + 64
