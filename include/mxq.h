@@ -154,6 +154,27 @@ mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, const uint8
 size_t mxq_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int fmt);
 
 /*
+ * mxq_gemm for callers that cannot allocate device memory when they call:
+ * code embedded in a host application that owns the device memory pool and
+ * passes a plug-in only its input and output buffers, or code running under a
+ * fixed memory budget that forbids per-call allocation.  The pages describe
+ * no such entry point; it exists only for these callers.
+ *
+ * Arguments and results are those of mxq_gemm, without the workspace: the
+ * scale scratch is a fixed 16 MiB device buffer inside the library, which
+ * every GPU that loads the library keeps until the process exits.  Problems
+ * whose mxq_gemm_workspace_size() exceeds 16 MiB are rejected with
+ * MXQ_ERR_WORKSPACE before any work is queued.  The call allocates nothing.
+ * The first call on each device looks up that device's address of the buffer
+ * (with the device current); make that first call before any stream capture.
+ * All calls share the buffer: calls that overlap on the GPU (other streams,
+ * other host threads) race on it and must be serialized by the caller.
+ */
+mxq_status mxq_gemm_noalloc(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                            int fmt, int64_t M, int64_t N, int64_t K, void* C, int out_dtype,
+                            void* stream);
+
+/*
  * Synchronizes `stream`, then reports and clears device-side errors recorded
  * by earlier calls on any stream (MXQ_ERR_TIMEOUT when a bounded wait inside
  * a kernel gave up), or MXQ_ERR_CUDA when the stream reports a CUDA error.

@@ -23,6 +23,8 @@
 // The row-major scales are first rewritten (a small pre-pass kernel) into
 // the tensor-core chunk layout in the caller's workspace: for every 128-row
 // x 4-block chunk, byte (r % 32) * 16 + (r / 32) * 4 + (kb % 4).
+#include <mutex>
+
 #include "mxq_common.cuh"
 #include "mxq_host.h"
 
@@ -500,4 +502,63 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   const int grid = std::min<int>(a.n_tiles, sm_count());
   mx_gemm_kernel<<<grid, G_THREADS, G_SMEM, st>>>(ta, tb, a);
   return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// GEMM without caller-provided scratch
+// ---------------------------------------------------------------------------
+// Some callers cannot allocate device memory at call time: code embedded in a
+// host application that owns the whole device memory pool and hands a plug-in
+// only its input and output buffers, or code that runs under a fixed memory
+// budget where allocating per call is forbidden.  For them the scale
+// re-layout scratch lives in one fixed buffer inside this library.
+//
+// The buffer is a file-scope device array of kNoAllocScratchBytes (16 MiB).
+// Every GPU that loads the library holds it until the process exits.  All
+// calls share it and it keeps the previous call's contents; each call
+// rewrites every byte it reads, so nothing needs clearing, but calls that
+// overlap on the GPU (two streams at once, or two host threads) race on it.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch for each device, taken once per device
+// with that device current (in host code the array's name is only a
+// host-side stand-in, not a device address).
+void* noalloc_scratch_ptr(mxq_status* st) {
+  static std::mutex mu;
+  static void* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *st = MXQ_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      *st = MXQ_ERR_CUDA;
+      return nullptr;
+    }
+    cache[dev] = p;
+  }
+  *st = MXQ_OK;
+  return cache[dev];
+}
+
+}  // namespace
+
+extern "C" mxq_status mxq_gemm_noalloc(const void* A, const uint8_t* sA, const void* B,
+                                       const uint8_t* sB, int fmt, int64_t M, int64_t N,
+                                       int64_t K, void* C, int out_dtype, void* stream) {
+  const size_t need = mxq_gemm_workspace_size(M, N, K, fmt);
+  if (need == 0) return MXQ_ERR_ARG;
+  if (need > kNoAllocScratchBytes) return MXQ_ERR_WORKSPACE;
+  mxq_status st;
+  void* scratch = noalloc_scratch_ptr(&st);
+  if (!scratch) return st;
+  return mxq_gemm(A, sA, B, sB, fmt, M, N, K, C, out_dtype, scratch, kNoAllocScratchBytes,
+                  stream);
 }

@@ -41,6 +41,7 @@ SIGNATURES = [
     ("mxq_dequantize", _I, [_P, _P, _I64, _I64, _I, _I, _P, _I, _P]),
     ("mxq_gemm", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P, _SZ, _P]),
     ("mxq_gemm_workspace_size", _SZ, [_I64, _I64, _I64, _I]),
+    ("mxq_gemm_noalloc", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P]),
     ("mxq_check", _I, [_P]),
     ("mxq_set_wait_timeout_ns", None, [_U64]),
     ("mxq_debug_expire_wait", _I, [_U64, _P]),
@@ -110,6 +111,11 @@ def mxq_dequantize(codes, scales, rows, cols, layout, fmt, out, out_dtype, strea
 
 def mxq_gemm(A, sA, B, sB, fmt, M, N, K, C, out_dtype, workspace, ws_bytes, stream):
     return lib().mxq_gemm(A, sA, B, sB, fmt, M, N, K, C, out_dtype, workspace, ws_bytes, stream)
+
+
+def mxq_gemm_noalloc(A, sA, B, sB, fmt, M, N, K, C, out_dtype, stream):
+    """mxq_gemm with the library's fixed internal scratch (for callers that cannot allocate)."""
+    return lib().mxq_gemm_noalloc(A, sA, B, sB, fmt, M, N, K, C, out_dtype, stream)
 
 
 def mxq_gemm_workspace_size(M, N, K, fmt):
