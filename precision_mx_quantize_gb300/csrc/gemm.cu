@@ -8,18 +8,24 @@
 // along K per MMA of K=32); E2M1 operands use kind::mxf4 on packed nibbles
 // (two scales per MMA of K=64).
 //
-// Kernel structure (one CTA per SM, persistent over 128x256 output tiles):
-//   warp 0     TMA producer: A tile 128 rows x 128 B and B tile 256 rows x
-//              128 B (128-byte swizzle) plus the stage's scale chunks (bulk
-//              copies) into a 4-stage shared-memory ring;
-//   warp 1     allocates the tensor memory; one lane copies the stage's
-//              scales shared->tensor memory (tcgen05.cp) and issues the four
-//              block-scaled MMAs of the stage into the fp32 accumulator
-//              (128 lanes x 256 columns), then commits the stage back to the
-//              producer;
-//   warps 2-9  epilogue: each drains 32 accumulator lanes x 128 columns into
-//              registers, frees the accumulator for the next tile, and
-//              stores its rows while the next tile's main loop runs.
+// Kernel structure: clusters of two CTAs on the two SMs of a TPC run the
+// pair MMA (cta_group::2) on 256x256 output tiles, persistent over tiles.
+// Each CTA holds 128 rows of A and 128 of the tile's 256 B rows; the pair
+// MMA reads both halves, so an SM streams 32 KB of operands per K stage
+// instead of the 48 KB a single-SM 128x256 tile needs, which keeps the
+// shared-memory traffic (TMA writes + tensor-core reads) within bandwidth.
+//   warp 0     (both CTAs) TMA producer: own A rows and own B half, 128 B of
+//              K per stage with 128-byte swizzle, plus the stage's scale
+//              chunks (own 128 A rows, all 256 B rows) into a 6-stage ring;
+//   warp 1     (both CTAs) allocates the pair's tensor memory.  In the
+//              leader CTA one lane copies each stage's scales into tensor
+//              memory (tcgen05.cp, both CTAs) and issues the four pair MMAs
+//              into the fp32 accumulators (each CTA: 128 lanes x 256
+//              columns), then releases the stage in both CTAs.  In the other
+//              CTA one lane forwards "stage loaded" to the leader;
+//   warps 2-9  (both CTAs) epilogue: each drains 32 accumulator lanes x 128
+//              columns into registers, tells the leader the accumulator is
+//              free, and stores its rows while the next tile's main loop runs.
 // The row-major scales are first rewritten (a small pre-pass kernel) into
 // the tensor-core chunk layout in the caller's workspace: for every 128-row
 // x 4-block chunk, byte (r % 32) * 16 + (r / 32) * 4 + (kb % 4).
@@ -34,53 +40,62 @@ __device__ uint32_t g_err_gemm;
 
 namespace {
 
-constexpr int G_BM = 128;                    // accumulator lanes (rows of A)
-constexpr int G_BN = 256;                    // accumulator columns (rows of B)
+constexpr int G_CLUSTER = 2;                 // CTA pair of one 2-SM MMA
+constexpr int G_BM = 128;                    // rows of A per CTA (pair tile: 256)
+constexpr int G_BN = 256;                    // columns of the tile (rows of B)
+constexpr int G_BN_CTA = G_BN / G_CLUSTER;   // rows of B each CTA holds
 constexpr int G_BKB = 128;                   // bytes of K per stage (one 128 B swizzle row)
-constexpr int G_STAGES = 4;
+constexpr int G_STAGES = 6;
 constexpr int G_THREADS = 320;               // 10 warps
 constexpr int G_A_BYTES = G_BM * G_BKB;      // 16 KB
-constexpr int G_B_BYTES = G_BN * G_BKB;      // 32 KB
-constexpr int G_SFA_BYTES = 1024;            // up to 2 chunks of 512 B
-constexpr int G_SFB_BYTES = 2048;            // up to 4 chunks of 512 B
+constexpr int G_B_BYTES = G_BN_CTA * G_BKB;  // 16 KB
+constexpr int G_SFA_BYTES = 1024;            // own 128 rows: up to 2 chunks of 512 B
+constexpr int G_SFB_BYTES = 2048;            // all 256 rows: up to 4 chunks of 512 B
 constexpr int G_STAGE_BYTES = G_A_BYTES + G_B_BYTES + G_SFA_BYTES + G_SFB_BYTES;
-constexpr int G_SMEM = G_STAGES * G_STAGE_BYTES + 1024 + 256;
+constexpr int G_BAR_BYTES = 256;
+constexpr int G_SMEM = G_STAGES * G_STAGE_BYTES + G_BAR_BYTES + 1024;
 constexpr uint32_t G_TMEM_COLS = 512;
-constexpr uint32_t G_SFA_COL0 = 256;         // 8 columns per stage
+constexpr uint32_t G_SFA_COL0 = 256;                 // 8 columns per stage
 constexpr uint32_t G_SFB_COL0 = 256 + 8 * G_STAGES;  // 16 columns per stage
+static_assert(G_SFB_COL0 + 16 * G_STAGES <= G_TMEM_COLS, "tensor memory budget");
+static_assert(G_STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 
 struct GArgs {
   int32_t M, N;
-  int32_t n_mt, n_nt, n_tiles;
-  int32_t nk;                 // K stages
-  int32_t kc_per_row;         // 512-byte scale chunks per 128-row tile (KBp / 4)
-  const uint8_t* sfa;         // chunked scales of A in the workspace
-  const uint8_t* sfb;         // chunked scales of B
+  int32_t n_mp, n_nt, n_tiles;  // 256-row pair tiles along M, 256-col tiles along N
+  int32_t nk;                   // K stages
+  int32_t kc_per_row;           // 512-byte scale chunks per 128-row tile (KBp / 4)
+  const uint8_t* sfa;           // chunked scales of A in the workspace
+  const uint8_t* sfb;           // chunked scales of B
   void* C;
   int32_t out_bf16;
   int32_t fp4;
   uint64_t timeout_ns;
 };
 
-// ---- tcgen05 wrappers ------------------------------------------------------
-MXQ_DEV void tmem_alloc(uint32_t dst_smem, uint32_t cols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+// ---- tcgen05 / cluster wrappers --------------------------------------------
+MXQ_DEV void tmem_alloc_pair(uint32_t dst_smem, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(cols)
                : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 
-MXQ_DEV void tmem_dealloc(uint32_t taddr, uint32_t cols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+MXQ_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
                : "memory");
 }
 
 MXQ_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 MXQ_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-MXQ_DEV void tc_commit(uint32_t bar) {
+// Arrive (once the pair's earlier tcgen05 operations complete) on the
+// barrier at `bar`'s offset in every CTA of cta_mask.
+MXQ_DEV void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 
@@ -96,35 +111,36 @@ MXQ_DEV uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t l
   return d;
 }
 
-// Copy one 512-byte scale chunk (32 rows x 16 B) into 4 tensor-memory
-// columns, replicated to all four 32-lane quadrants.
-MXQ_DEV void tc_cp_sf(uint32_t taddr, uint32_t smem_addr) {
+// Copy one 512-byte scale chunk (32 rows x 16 B) of each CTA's shared memory
+// into 4 columns of the same CTA's tensor memory, replicated to all four
+// 32-lane quadrants.
+MXQ_DEV void tc_cp_sf_pair(uint32_t taddr, uint32_t smem_addr) {
   const uint64_t d = smem_desc(smem_addr, 0, 128, 0);
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
 }
 
-MXQ_DEV void mma_mxf8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                      uint32_t sfb, uint32_t accum) {
+MXQ_DEV void mma_mxf8_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                           uint32_t sfb, uint32_t accum) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], "
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], "
       "[%6], p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb)
       : "memory");
 }
 
-MXQ_DEV void mma_mxf4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                      uint32_t sfb, uint32_t accum) {
+MXQ_DEV void mma_mxf4_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                           uint32_t sfb, uint32_t accum) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], "
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], "
       "[%6], p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb)
       : "memory");
 }
 
-// Instruction descriptor of a block-scaled MMA: K-major A and B, M = 128,
-// N = 256, E8M0 scales, scale-factor byte ids a_sf / b_sf.
+// Instruction descriptor of a block-scaled pair MMA: K-major A and B,
+// M = 256 (128 per CTA), N = 256, E8M0 scales, scale-factor byte ids.
 MXQ_DEV uint32_t idesc_block_scaled(uint32_t fmt_code, uint32_t a_sf, uint32_t b_sf) {
   uint32_t d = 0;
   d |= (b_sf & 3u) << 4;
@@ -132,7 +148,7 @@ MXQ_DEV uint32_t idesc_block_scaled(uint32_t fmt_code, uint32_t a_sf, uint32_t b
   d |= (fmt_code & 7u) << 10;   // B format
   d |= static_cast<uint32_t>(G_BN >> 3) << 17;
   d |= 1u << 23;                // scale type: UE8M0
-  d |= static_cast<uint32_t>(G_BM >> 4) << 24;
+  d |= static_cast<uint32_t>((G_CLUSTER * G_BM) >> 4) << 24;
   d |= (a_sf & 3u) << 29;
   return d;
 }
@@ -151,11 +167,48 @@ MXQ_DEV uint32_t idesc_block_scaled(uint32_t fmt_code, uint32_t a_sf, uint32_t b
 
 MXQ_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// A bounded wait that also gives up once another role has aborted.
+MXQ_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+MXQ_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+MXQ_DEV uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on a barrier that may live in another CTA of the cluster.
+MXQ_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+MXQ_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// A bounded wait (cluster-scope acquire) that also gives up once another
+// role of this CTA has aborted.
 MXQ_DEV bool gwait(uint32_t bar, uint32_t parity, uint64_t limit, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_cluster(bar, parity)) {
     if (*abort_flag) return false;
     if (global_ns() - t0 > limit) return false;
   }
@@ -167,8 +220,20 @@ MXQ_DEV void gabort(volatile int* abort_flag, uint32_t site) {
   record_error(&g_err_gemm, MXQ_ERR_TIMEOUT, site);
 }
 
+// TMA load whose completion is signalled on a barrier that may live in the
+// peer CTA of the pair (`bar` is a cluster shared-memory address).
+MXQ_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                              int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
 __global__ void __launch_bounds__(G_THREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                    const GArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -176,143 +241,168 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G_STAGES * G_STAGE_BYTES);
   uint64_t* empty = full + G_STAGES;
   uint64_t* tmem_full = empty + G_STAGES;
-  uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* tmem_empty = tmem_full + 1;      // leader: both CTAs drained the accumulator
   uint64_t* drain = tmem_empty + 1;
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSA);
+    prefetch_tmap(&tmSB);
     for (int s = 0; s < G_STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&full[s]), 1);    // leader: one arrival, bytes of both CTAs
       mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(tmem_full), 1);
-    mbar_init(smem_u32(tmem_empty), 8);
+    mbar_init(smem_u32(tmem_empty), 8 * G_CLUSTER);
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_base_slot), G_TMEM_COLS);
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_base_slot), G_TMEM_COLS);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of both CTAs exist before anyone signals the peer
   tc_fence_after();
+  const int cid = blockIdx.x / G_CLUSTER, ncl = gridDim.x / G_CLUSTER;
   const uint32_t tmem = *tmem_base_slot;
+  const int n_tiles = a.n_tiles, n_nt = a.n_nt, nk = a.nk;
+  const uint64_t tmo = a.timeout_ns;
 
-  const int n_sfa = a.fp4 ? 2 : 1;            // 512-byte chunks of A scales per stage
+  const int n_sfa = a.fp4 ? 2 : 1;            // 512-byte chunks of own-A scales per stage
   const uint32_t sf_bytes_a = 512u * n_sfa;   // per 128 rows
-  const uint32_t stage_tx = G_A_BYTES + G_B_BYTES + 3 * sf_bytes_a;
+  // bytes one CTA brings into a stage; the leader's barrier counts both CTAs
+  const uint32_t cta_tx = G_A_BYTES + G_B_BYTES + 3 * sf_bytes_a;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (both CTAs) ----------------
     if (lane == 0) {
-      uint32_t it = 0;
+      // every load of both CTAs completes on the leader's stage barrier
+      const uint32_t full0 = map_to_rank(smem_u32(&full[0]), 0);
+      uint32_t s = 0, phase = 0, issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x) {
-        const int mt = t / a.n_nt, nt = t - mt * a.n_nt;
-        for (int ks = 0; ks < a.nk; ++ks, ++it) {
-          const uint32_t s = it % G_STAGES;
-          if (!gwait(smem_u32(&empty[s]), ((it / G_STAGES) & 1) ^ 1, a.timeout_ns, abort_flag)) {
+      for (int t = cid; t < n_tiles && ok; t += ncl) {
+        const int nt = t % n_nt, mp = t / n_nt;
+        const int mt = G_CLUSTER * mp + static_cast<int>(rank);   // this CTA's 128-row tile
+        const int srow_a = mt * a.kc_per_row;                     // first scale chunk rows
+        const int srow_b0 = (2 * nt) * a.kc_per_row, srow_b1 = (2 * nt + 1) * a.kc_per_row;
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_try_wait_cluster(smem_u32(&empty[s]), phase ^ 1) &&
+              !gwait(smem_u32(&empty[s]), phase ^ 1, tmo, abort_flag)) {
             if (!*abort_flag) gabort(abort_flag, SITE_GEMM_EMPTY);
             ok = false;
             break;
           }
-          uint8_t* st = smem + s * G_STAGE_BYTES;
-          const uint32_t bar = smem_u32(&full[s]);
-          mbar_arrive_expect_tx(bar, stage_tx);
-          tma_load_2d(smem_u32(st), &tmA, bar, ks * G_BKB, mt * G_BM);
-          tma_load_2d(smem_u32(st + G_A_BYTES), &tmB, bar, ks * G_BKB, nt * G_BN);
-          const int kc = ks * n_sfa;  // first 512-byte chunk column of this stage
-          const uint8_t* srcA = a.sfa + (int64_t(mt) * a.kc_per_row + kc) * 512;
-          bulk_load(smem_u32(st + G_A_BYTES + G_B_BYTES), srcA, sf_bytes_a, bar);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint8_t* srcB = a.sfb + (int64_t(2 * nt + h) * a.kc_per_row + kc) * 512;
-            bulk_load(smem_u32(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES + h * sf_bytes_a), srcB,
-                      sf_bytes_a, bar);
-          }
+          const uint32_t st = smem_u32(smem + s * G_STAGE_BYTES);
+          const uint32_t bar = full0 + s * 8;
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), G_CLUSTER * cta_tx);
+          tma_load_2d_pair(st, &tmA, bar, ks * G_BKB, mt * G_BM);
+          tma_load_2d_pair(st + G_A_BYTES, &tmB, bar, ks * G_BKB,
+                           nt * G_BN + static_cast<int>(rank) * G_BN_CTA);
+          const int kc = ks * n_sfa;
+          tma_load_2d_pair(st + G_A_BYTES + G_B_BYTES, &tmSA, bar, 0, srow_a + kc);
+          tma_load_2d_pair(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES, &tmSB, bar, 0, srow_b0 + kc);
+          tma_load_2d_pair(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES + sf_bytes_a, &tmSB, bar, 0,
+                           srow_b1 + kc);
+          ++issued;
+          if (++s == G_STAGES) { s = 0; phase ^= 1; }
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         // bounded wait for the copies of the stages issued last
-        for (int s = 0; s < G_STAGES; ++s) {
-          if (it >= uint32_t(s + 1)) {
-            const uint32_t k = it - 1 - s;
-            gwait(smem_u32(&full[k % G_STAGES]), (k / G_STAGES) & 1, a.timeout_ns, abort_flag);
-          }
-        }
+        for (uint32_t k = issued > G_STAGES ? issued - G_STAGES : 0; k < issued; ++k)
+          mbar_wait(smem_u32(&full[k % G_STAGES]), (k / G_STAGES) & 1, tmo);
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    if (lane == 0 && leader) {
+      // ---------------- pair-MMA issuer (leader CTA) ----------------
+      // Everything that does not change per stage is computed once: each
+      // tcgen05 instruction costs the issuing thread ~100 cycles, so the
+      // loop keeps nothing else on its path.
       const uint32_t fmt_code = a.fp4 ? 1u : 0u;  // kind::mxf4 E2M1 = 1, kind::mxf8f6f4 E4M3 = 0
-      uint32_t it = 0, tile_i = 0;
+      uint32_t idesc[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t sf_id = a.fp4 ? ((2 * j) & 3) : j;
+        idesc[j] = idesc_block_scaled(fmt_code, sf_id, sf_id);
+      }
+      const uint32_t st0 = smem_u32(smem);
+      const uint64_t adesc_s0 = smem_desc(st0, 0, 1024, 2);
+      const uint64_t bdesc_s0 = smem_desc(st0 + G_A_BYTES, 0, 1024, 2);
+      constexpr uint32_t kStageDesc = G_STAGE_BYTES >> 4;   // stage stride in descriptor units
+      const bool fp4 = a.fp4 != 0;
+      uint32_t s = 0, phase = 0, tile_i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x, ++tile_i) {
-        if (!gwait(smem_u32(tmem_empty), (tile_i & 1) ^ 1, a.timeout_ns, abort_flag)) {
+      for (int t = cid; t < n_tiles && ok; t += ncl, ++tile_i) {
+        if (!mbar_try_wait_cluster(smem_u32(tmem_empty), (tile_i & 1) ^ 1) &&
+            !gwait(smem_u32(tmem_empty), (tile_i & 1) ^ 1, tmo, abort_flag)) {
           if (!*abort_flag) gabort(abort_flag, SITE_GEMM_TMEM_EMPTY);
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int ks = 0; ks < a.nk; ++ks, ++it) {
-          const uint32_t s = it % G_STAGES;
-          if (!gwait(smem_u32(&full[s]), (it / G_STAGES) & 1, a.timeout_ns, abort_flag)) {
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_try_wait_cluster(smem_u32(&full[s]), phase) &&
+              !gwait(smem_u32(&full[s]), phase, tmo, abort_flag)) {
             if (!*abort_flag) gabort(abort_flag, SITE_GEMM_FULL);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + s * G_STAGE_BYTES);
-          const uint32_t sfa_smem = st + G_A_BYTES + G_B_BYTES;
+          const uint32_t sfa_smem = st0 + s * G_STAGE_BYTES + G_A_BYTES + G_B_BYTES;
           const uint32_t sfb_smem = sfa_smem + G_SFA_BYTES;
-          const uint32_t sfa_col = G_SFA_COL0 + 8 * s;
-          const uint32_t sfb_col = G_SFB_COL0 + 16 * s;
-          // scales -> tensor memory.  A: chunk c -> columns sfa_col + 4c.
-          // B: k-chunk c of rows 0-127 -> sfb_col + 8c, rows 128-255 -> +4.
-          for (int c = 0; c < n_sfa; ++c) {
-            tc_cp_sf(tmem + sfa_col + 4 * c, sfa_smem + 512 * c);
-            tc_cp_sf(tmem + sfb_col + 8 * c, sfb_smem + 512 * c);
-            tc_cp_sf(tmem + sfb_col + 8 * c + 4, sfb_smem + sf_bytes_a + 512 * c);
+          const uint32_t sfa_t = tmem + G_SFA_COL0 + 8 * s;
+          const uint32_t sfb_t = tmem + G_SFB_COL0 + 16 * s;
+          const uint64_t ad = adesc_s0 + s * kStageDesc;
+          const uint64_t bd = bdesc_s0 + s * kStageDesc;
+          // scales -> tensor memory of both CTAs.  A (own rows): chunk c ->
+          // columns +4c.  B: k-chunk c of rows 0-127 -> +8c, rows 128-255 -> +8c+4.
+          if (fp4) {
+            tc_cp_sf_pair(sfa_t, sfa_smem);
+            tc_cp_sf_pair(sfa_t + 4, sfa_smem + 512);
+            tc_cp_sf_pair(sfb_t, sfb_smem);
+            tc_cp_sf_pair(sfb_t + 8, sfb_smem + 512);
+            tc_cp_sf_pair(sfb_t + 4, sfb_smem + 1024);
+            tc_cp_sf_pair(sfb_t + 12, sfb_smem + 1536);
+            // each MMA consumes 32 bytes of K (K=64 packed E2M1), k-blocks 2j, 2j+1
+            mma_mxf4_pair(tmem, ad, bd, idesc[0], sfa_t, sfb_t, ks > 0 ? 1u : 0u);
+            mma_mxf4_pair(tmem, ad + 2, bd + 2, idesc[1], sfa_t, sfb_t, 1u);
+            mma_mxf4_pair(tmem, ad + 4, bd + 4, idesc[2], sfa_t + 4, sfb_t + 8, 1u);
+            mma_mxf4_pair(tmem, ad + 6, bd + 6, idesc[3], sfa_t + 4, sfb_t + 8, 1u);
+          } else {
+            tc_cp_sf_pair(sfa_t, sfa_smem);
+            tc_cp_sf_pair(sfb_t, sfb_smem);
+            tc_cp_sf_pair(sfb_t + 4, sfb_smem + 512);
+            // each MMA consumes 32 bytes of K (K=32 E4M3), k-block j
+            mma_mxf8_pair(tmem, ad, bd, idesc[0], sfa_t, sfb_t, ks > 0 ? 1u : 0u);
+            mma_mxf8_pair(tmem, ad + 2, bd + 2, idesc[1], sfa_t, sfb_t, 1u);
+            mma_mxf8_pair(tmem, ad + 4, bd + 4, idesc[2], sfa_t, sfb_t, 1u);
+            mma_mxf8_pair(tmem, ad + 6, bd + 6, idesc[3], sfa_t, sfb_t, 1u);
           }
-          const uint64_t adesc0 = smem_desc(st, 0, 1024, 2);
-          const uint64_t bdesc0 = smem_desc(st + G_A_BYTES, 0, 1024, 2);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // each MMA consumes 32 bytes of K: K=32 E4M3 or K=64 packed E2M1
-            const uint64_t ad = adesc0 + static_cast<uint64_t>((32 * j) >> 4);
-            const uint64_t bd = bdesc0 + static_cast<uint64_t>((32 * j) >> 4);
-            const uint32_t accum = (ks > 0 || j > 0) ? 1u : 0u;
-            if (a.fp4) {
-              const uint32_t sf_id = (2 * j) & 3;           // k-blocks 2j, 2j+1
-              const uint32_t chunk = (2 * j) >> 2;
-              mma_mxf4(tmem, ad, bd, idesc_block_scaled(fmt_code, sf_id, sf_id),
-                       tmem + sfa_col + 4 * chunk, tmem + sfb_col + 8 * chunk, accum);
-            } else {
-              mma_mxf8(tmem, ad, bd, idesc_block_scaled(fmt_code, j, j), tmem + sfa_col,
-                       tmem + sfb_col, accum);
-            }
-          }
-          tc_commit(smem_u32(&empty[s]));
+          tc_commit_pair_mc(smem_u32(&empty[s]), 0x3);   // stage free in both CTAs
+          if (++s == G_STAGES) { s = 0; phase ^= 1; }
         }
         if (!ok) break;
-        tc_commit(smem_u32(tmem_full));
+        tc_commit_pair_mc(smem_u32(tmem_full), 0x3);     // accumulators ready in both CTAs
       }
-      // all MMAs issued by this thread are complete before teardown
-      tc_commit(smem_u32(drain));
-      if (!mbar_wait(smem_u32(drain), 0, a.timeout_ns))
+      // all pair MMAs issued by this thread are complete before teardown
+      tc_commit_pair_mc(smem_u32(drain), 0x1);
+      if (!mbar_wait(smem_u32(drain), 0, tmo))
         record_error(&g_err_gemm, MXQ_ERR_TIMEOUT, SITE_GEMM_DRAIN);
     }
   } else {
-    // ---------------- epilogue (warps 2..9) ----------------
+    // ---------------- epilogue (warps 2..9, both CTAs) ----------------
     const int quad = warp & 3;                   // tensor-memory lane quadrant
     const int colh = (warp - 2) >> 2;            // 0: columns 0-127, 1: 128-255
+    const uint32_t empty_leader = map_to_rank(smem_u32(tmem_empty), 0);
     uint32_t tile_i = 0;
-    for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++tile_i) {
-      if (!gwait(smem_u32(tmem_full), tile_i & 1, a.timeout_ns, abort_flag)) {
+    for (int t = cid; t < n_tiles; t += ncl, ++tile_i) {
+      if (!gwait(smem_u32(tmem_full), tile_i & 1, tmo, abort_flag)) {
         if (lane == 0 && !*abort_flag) gabort(abort_flag, SITE_GEMM_TMEM_FULL);
         break;
       }
@@ -326,10 +416,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(tmem_empty));
+      if (lane == 0) mbar_arrive_cluster(empty_leader);
 
-      const int mt = t / a.n_nt, nt = t - mt * a.n_nt;
-      const int64_t row = int64_t(mt) * G_BM + quad * 32 + lane;
+      const int nt = t % n_nt, mp = t / n_nt;
+      const int64_t row = (int64_t(mp) * G_CLUSTER + rank) * G_BM + quad * 32 + lane;
       const int64_t col0 = int64_t(nt) * G_BN + colh * 128;
       if (row < a.M && col0 < a.N) {
         const int64_t ncols = (a.N - col0) < 128 ? (a.N - col0) : 128;
@@ -361,9 +451,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, G_TMEM_COLS);
+  if (warp == 1) tmem_dealloc_pair(tmem, G_TMEM_COLS);
 }
 
 // Row-major E8M0 scales [rows][kb] -> chunked tensor-core layout, zero padded
@@ -403,11 +493,31 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int fmt, Plan& p) {
   p.kb = K / 32;
   p.skb = fmt == MXQ_E4M3 ? 4 : 8;  // k-blocks per 128-byte stage
   p.kbp = (p.kb + p.skb - 1) / p.skb * p.skb;
-  p.mp = (M + G_BM - 1) / G_BM * G_BM;
+  p.mp = (M + G_CLUSTER * G_BM - 1) / (G_CLUSTER * G_BM) * (G_CLUSTER * G_BM);
   p.np = (N + G_BN - 1) / G_BN * G_BN;
   p.ws_a = p.mp * p.kbp;
   p.ws_b = p.np * p.kbp;
   return true;
+}
+
+// Clusters of G_CLUSTER GEMM CTAs that fit on the device at once (cached per
+// device).
+int max_gemm_clusters(cudaLaunchConfig_t cfg) {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    cfg.gridDim = dim3(static_cast<unsigned>(G_CLUSTER * sm_count()), 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = sm_count() / G_CLUSTER;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 }  // namespace
@@ -473,20 +583,40 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.kbytes), static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.kbytes)};
-    const cuuint32_t box[2] = {G_BKB, G_BN};
+    const cuuint32_t box[2] = {G_BKB, G_BN_CTA};
     if (encode(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(B), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MXQ_ERR_CUDA;
   }
 
+  // Scale chunks as 2-D tensors of 512-byte rows (128 x uint32), one row per
+  // (128-row tile, k-chunk): a stage loads n_sfa consecutive rows.
+  CUtensorMap tsa, tsb;
+  {
+    const int n_sfa = fmt == MXQ_E2M1 ? 2 : 1;
+    const int64_t kcs = p.kbp / 4;
+    for (int which = 0; which < 2; ++which) {
+      const int64_t rows = (which == 0 ? p.mp : p.np) / G_BM * kcs;
+      const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+      const cuuint64_t strides[1] = {512};
+      const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(n_sfa)};
+      if (encode(which == 0 ? &tsa : &tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
+                 ws + (which == 0 ? 0 : p.ws_a), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MXQ_ERR_CUDA;
+    }
+  }
+
   GArgs a;
   a.M = static_cast<int32_t>(M);
   a.N = static_cast<int32_t>(N);
-  a.n_mt = static_cast<int32_t>(p.mp / G_BM);
+  a.n_mp = static_cast<int32_t>(p.mp / (G_CLUSTER * G_BM));
   a.n_nt = static_cast<int32_t>(p.np / G_BN);
-  if (int64_t(a.n_mt) * a.n_nt >= (int64_t(1) << 31)) return MXQ_ERR_ARG;
-  a.n_tiles = a.n_mt * a.n_nt;
+  // one work item = one 256x256 pair tile (one cluster)
+  if (int64_t(a.n_mp) * a.n_nt >= (int64_t(1) << 31)) return MXQ_ERR_ARG;
+  a.n_tiles = a.n_mp * a.n_nt;
   a.nk = static_cast<int32_t>((p.kbytes + G_BKB - 1) / G_BKB);
   a.kc_per_row = static_cast<int32_t>(p.kbp / 4);
   a.sfa = ws;
@@ -499,8 +629,21 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(mx_gemm_kernel),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM) != cudaSuccess)
     return MXQ_ERR_CUDA;
-  const int grid = std::min<int>(a.n_tiles, sm_count());
-  mx_gemm_kernel<<<grid, G_THREADS, G_SMEM, st>>>(ta, tb, a);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = G_CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(G_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = G_SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int max_clusters = max_gemm_clusters(cfg);
+  if (max_clusters <= 0) return MXQ_ERR_CUDA;
+  cfg.gridDim = dim3(static_cast<unsigned>(G_CLUSTER * std::min(a.n_tiles, max_clusters)), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, mx_gemm_kernel, ta, tb, tsa, tsb, a) != cudaSuccess) return MXQ_ERR_CUDA;
   return launch_status();
 }
 

@@ -143,7 +143,8 @@ def test_gemm_argument_errors():
     assert mxq.mxq_gemm(p, p, p, p, 0, 128, 130, 64, p, 0, p, 1 << 20, s) == 2   # N % 4
     assert mxq.mxq_gemm(p, p, p, p, 0, 128, 128, 64, p, 0, p, 16, s) == 6        # workspace
     assert mxq.mxq_gemm(p, p, p, p, 5, 128, 128, 64, p, 0, p, 1 << 20, s) == 1   # fmt
-    assert mxq.mxq_gemm_workspace_size(128, 256, 4096, 0) == 128 * 128 + 256 * 128
+    # scales padded to 256 rows for A (a pair of m-tiles) and B (one n-tile)
+    assert mxq.mxq_gemm_workspace_size(128, 256, 4096, 0) == 256 * 128 + 256 * 128
 
 
 def _sample_idx(n, rng, k=192):
