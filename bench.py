@@ -204,36 +204,45 @@ def build_device_state(plan, device):
 LAUNCHES_PER_LAYER = 3 + 3 * 3
 
 
+def run_layer(st, mark=None):
+    """Enqueue one layer's dual quantizers and its three GEMMs on the current stream."""
+    import torch
+
+    from precision_mx_quantize_gb300 import mxq
+    T, fin, fout = st["L"]["T"], st["L"]["fin"], st["L"]["fout"]
+    if mark:
+        mark("q")
+    mxq.mx_quantize_dual(st["x"], "e4m3", False, "e2m1", True, out=st["xq"])
+    mxq.mx_quantize_dual(st["w"], "e4m3", False, "e4m3", False, out=st["wq"])
+    mxq.mx_quantize_dual(st["dy"], "e4m3", False, "e2m1", True, out=st["dyq"])
+    if mark:
+        mark("f8")
+    xr, sxr, xc, sxc = st["xq"]
+    wr, swr, wc, swc = st["wq"]
+    dr, sdr, dc, sdc = st["dyq"]
+    mxq.mx_gemm(xr, sxr, wr, swr, "e4m3", T, fout, fin, torch.bfloat16, out=st["y"],
+                workspace=st["ws_f"])
+    mxq.mx_gemm(dr, sdr, wc, swc, "e4m3", T, fin, fout, torch.bfloat16, out=st["dx"],
+                workspace=st["ws_d"])
+    if mark:
+        mark("f4")
+    mxq.mx_gemm(dc, sdc, xc, sxc, "e2m1", fout, fin, T, torch.float32, out=st["dw"],
+                workspace=st["ws_w"])
+
+
 def run_step(layers, events=None):
     """Enqueue one pass of the hot path on the current stream."""
     import torch
 
-    from precision_mx_quantize_gb300 import mxq
-
     def mark(tag):
-        if events is not None:
-            e = torch.cuda.Event(enable_timing=True)
-            e.record()
-            events.append((tag, e))
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        events.append((tag, e))
 
     for st in layers:
-        T, fin, fout = st["L"]["T"], st["L"]["fin"], st["L"]["fout"]
-        mark("q")
-        mxq.mx_quantize_dual(st["x"], "e4m3", False, "e2m1", True, out=st["xq"])
-        mxq.mx_quantize_dual(st["w"], "e4m3", False, "e4m3", False, out=st["wq"])
-        mxq.mx_quantize_dual(st["dy"], "e4m3", False, "e2m1", True, out=st["dyq"])
-        mark("f8")
-        xr, sxr, xc, sxc = st["xq"]
-        wr, swr, wc, swc = st["wq"]
-        dr, sdr, dc, sdc = st["dyq"]
-        mxq.mx_gemm(xr, sxr, wr, swr, "e4m3", T, fout, fin, torch.bfloat16, out=st["y"],
-                    workspace=st["ws_f"])
-        mxq.mx_gemm(dr, sdr, wc, swc, "e4m3", T, fin, fout, torch.bfloat16, out=st["dx"],
-                    workspace=st["ws_d"])
-        mark("f4")
-        mxq.mx_gemm(dc, sdc, xc, sxc, "e2m1", fout, fin, T, torch.float32, out=st["dw"],
-                    workspace=st["ws_w"])
-    mark("end")
+        run_layer(st, mark if events is not None else None)
+    if events is not None:
+        mark("end")
 
 
 def interval_sums(events):
@@ -374,18 +383,40 @@ def gpu_arm(args, rank, world, local_rank):
 
 
 def _profile_traffic():
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if any."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per MXFP8 GEMM launch of this step, from the committed ncu summary.
+
+    The summary records the sha256 of the GEMM source it was captured from;
+    once the source changes the number no longer describes this kernel and
+    None is returned.
+    """
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "mx_gemm_kernel_dram_llama8b_block.md")
+    src = os.path.join(ROOT, "precision_mx_quantize_gb300", "csrc", "gemm.cu")
     try:
-        with open(path) as f:
-            return json.load(f).get("mx_gemm_kernel_e4m3_bytes_per_launch")
+        fields = {}
+        with open(prof) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith("- "):
+                    k, _, v = line.strip()[2:].partition(":")
+                    fields[k.strip().strip("`")] = v.strip().strip("`")
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        if fields.get("gemm_source_sha256") != digest:
+            return None
+        return int(fields["mxfp8_dram_bytes_per_launch"])
     except Exception:
         return None
 
 
 def e2e_measure(args, layers, flops, device):
-    """Same step through the public API with pinned host inputs copied in and
-    the Wgrad outputs (the step's gradients) copied back, inside the timed region."""
+    """The same step through the public API with host buffers.
+
+    Every step copies all of its bf16 inputs (X, W, dY of every layer) from
+    pinned host memory to the device and copies the step's gradients (dW of
+    every layer, fp32) back, inside the timed region.  Copies run on their own
+    streams so that layer i+1's inputs and layer i-1's gradients move while
+    layer i computes; events order every buffer reuse.
+    """
     import torch
     host_in, host_out = [], []
     h2d = d2h = 0
@@ -396,30 +427,56 @@ def e2e_measure(args, layers, flops, device):
         ho = torch.empty(st["dw"].shape, dtype=st["dw"].dtype, pin_memory=True)
         host_out.append(ho)
         d2h += ho.numel() * ho.element_size()
+    compute = torch.cuda.current_stream(device)
+    up = torch.cuda.Stream(device)
+    down = torch.cuda.Stream(device)
+    n = len(layers)
+    # inputs of layer i may be overwritten once the previous step's layer i
+    # computed; dW of layer i may be overwritten once it was copied back
+    done_compute = [torch.cuda.Event() for _ in range(n)]
+    done_down = [torch.cuda.Event() for _ in range(n)]
+    for i in range(n):
+        done_compute[i].record(compute)
+        done_down[i].record(compute)
 
     def one():
-        for st, hi, ho in zip(layers, host_in, host_out):
-            st["x"].copy_(hi["x"], non_blocking=True)
-            st["w"].copy_(hi["w"], non_blocking=True)
-            st["dy"].copy_(hi["dy"], non_blocking=True)
-        run_step(layers)
-        for st, ho in zip(layers, host_out):
-            ho.copy_(st["dw"], non_blocking=True)
+        arrived = []
+        for i, (st, hi) in enumerate(zip(layers, host_in)):
+            with torch.cuda.stream(up):
+                up.wait_event(done_compute[i])
+                st["x"].copy_(hi["x"], non_blocking=True)
+                st["w"].copy_(hi["w"], non_blocking=True)
+                st["dy"].copy_(hi["dy"], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(up)
+                arrived.append(ev)
+        for i, st in enumerate(layers):
+            compute.wait_event(arrived[i])
+            compute.wait_event(done_down[i])
+            run_layer(st)
+            done_compute[i].record(compute)
+            with torch.cuda.stream(down):
+                down.wait_event(done_compute[i])
+                host_out[i].copy_(st["dw"], non_blocking=True)
+                done_down[i].record(down)
 
-    steps = max(1, min(args.steps, 5))
+    steps = max(1, min(args.steps, 10))
     one()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
+    t0.record(compute)
     for _ in range(steps):
         one()
-    t1.record()
+    for i in range(n):
+        compute.wait_event(done_down[i])
+    t1.record(compute)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "overlap": "H2D, compute and D2H on separate streams, ordered per layer by events"}
 
 
 # ---------------------------------------------------------------------------
@@ -458,7 +515,7 @@ def _oracle_sample_step(plan, t_s, out_s, seed=0):
 
 
 def cpu_baseline(budget_s=15.0):
-    t_s, out_s = 256, 1024
+    t_s, out_s = 512, 2048
     plan = layer_plan(8192)
     t0 = time.perf_counter()
     flops = _oracle_sample_step(plan, t_s, out_s)
@@ -500,6 +557,46 @@ def reference_arm(args, rank, world):
     }
 
 
+CASES = {
+    # name: (what, args) -- one small, self-contained launch sequence for ncu
+    "gemm-e4m3": ("gemm", (8192, 8192, 4096, "e4m3", "f32")),
+    "gemm-e2m1": ("gemm", (8192, 8192, 8192, "e2m1", "bf16")),
+    "quant-dual-e4m3-he2m1": ("quant", (16384, 8192, "e4m3", False, "e2m1", True)),
+    "quant-dual-he2m1-he2m1": ("quant", (16384, 8192, "e2m1", True, "e2m1", True)),
+}
+
+
+def run_case(name):
+    """Run one kernel case three times (for ncu captures of a single kernel)."""
+    import torch
+
+    from precision_mx_quantize_gb300 import mxq
+    what, args = CASES[name]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    if what == "gemm":
+        M, N, K, fmt, od = args
+        kb = K if fmt == "e4m3" else K // 2
+        hi = 0x7E if fmt == "e4m3" else 256
+        A = torch.randint(0, hi, (M, kb), dtype=torch.uint8, device="cuda", generator=g)
+        B = torch.randint(0, hi, (N, kb), dtype=torch.uint8, device="cuda", generator=g)
+        sA = torch.randint(120, 134, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
+        sB = torch.randint(120, 134, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
+        dt = torch.float32 if od == "f32" else torch.bfloat16
+        C = torch.empty((M, N), dtype=dt, device="cuda")
+        ws = mxq.gemm_workspace(M, N, K, fmt, "cuda")
+        for _ in range(3):
+            mxq.mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=dt, out=C, workspace=ws)
+    else:
+        R, Cc, fr, hr, fc, hc = args
+        x = torch.randn(R, Cc, device="cuda", generator=g).to(torch.bfloat16)
+        out = mxq.mx_quantize_dual(x, fr, hr, fc, hc)
+        for _ in range(2):
+            mxq.mx_quantize_dual(x, fr, hr, fc, hc, out=out)
+    mxq.check()
+    print(json.dumps({"case": name, "status": "ok"}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -509,7 +606,11 @@ def main():
     ap.add_argument("--tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--case", choices=sorted(CASES), help="run one kernel case (for ncu) and exit")
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case)
+        return
     args.warmup = max(3, args.warmup)
 
     world = _env_int("WORLD_SIZE", 1)

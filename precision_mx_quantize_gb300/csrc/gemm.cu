@@ -18,14 +18,15 @@
 //              K per stage with 128-byte swizzle, plus the stage's scale
 //              chunks (own 128 A rows, all 256 B rows) into a 6-stage ring;
 //   warp 1     (both CTAs) allocates the pair's tensor memory.  In the
-//              leader CTA one lane copies each stage's scales into tensor
-//              memory (tcgen05.cp, both CTAs) and issues the four pair MMAs
+//              leader CTA one lane issues the four pair MMAs of each stage
 //              into the fp32 accumulators (each CTA: 128 lanes x 256
-//              columns), then releases the stage in both CTAs.  In the other
-//              CTA one lane forwards "stage loaded" to the leader;
+//              columns), then releases the stage in both CTAs;
+//   warp 10    (leader) one lane copies each stage's scales into both CTAs'
+//              tensor memory (tcgen05.cp) ahead of the MMA lane;
 //   warps 2-9  (both CTAs) epilogue: each drains 32 accumulator lanes x 128
 //              columns into registers, tells the leader the accumulator is
-//              free, and stores its rows while the next tile's main loop runs.
+//              free, and stores its rows (256-bit stores when aligned) while
+//              the next tile's main loop runs.
 // The row-major scales are first rewritten (a small pre-pass kernel) into
 // the tensor-core chunk layout in the caller's workspace: for every 128-row
 // x 4-block chunk, byte (r % 32) * 16 + (r / 32) * 4 + (kb % 4).
@@ -46,13 +47,13 @@ constexpr int G_BN = 256;                    // columns of the tile (rows of B)
 constexpr int G_BN_CTA = G_BN / G_CLUSTER;   // rows of B each CTA holds
 constexpr int G_BKB = 128;                   // bytes of K per stage (one 128 B swizzle row)
 constexpr int G_STAGES = 6;
-constexpr int G_THREADS = 320;               // 10 warps
+constexpr int G_THREADS = 352;               // 11 warps
 constexpr int G_A_BYTES = G_BM * G_BKB;      // 16 KB
 constexpr int G_B_BYTES = G_BN_CTA * G_BKB;  // 16 KB
 constexpr int G_SFA_BYTES = 1024;            // own 128 rows: up to 2 chunks of 512 B
 constexpr int G_SFB_BYTES = 2048;            // all 256 rows: up to 4 chunks of 512 B
 constexpr int G_STAGE_BYTES = G_A_BYTES + G_B_BYTES + G_SFA_BYTES + G_SFB_BYTES;
-constexpr int G_BAR_BYTES = 256;
+constexpr int G_BAR_BYTES = 512;
 constexpr int G_SMEM = G_STAGES * G_STAGE_BYTES + G_BAR_BYTES + 1024;
 constexpr uint32_t G_TMEM_COLS = 512;
 constexpr uint32_t G_SFA_COL0 = 256;                 // 8 columns per stage
@@ -70,6 +71,7 @@ struct GArgs {
   void* C;
   int32_t out_bf16;
   int32_t fp4;
+  int32_t wide_stores;          // rows of C are 32-byte aligned: 256-bit stores
   uint64_t timeout_ns;
 };
 
@@ -165,6 +167,14 @@ MXQ_DEV uint32_t idesc_block_scaled(uint32_t fmt_code, uint32_t a_sf, uint32_t b
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
       : "r"(taddr))
 
+// 256-bit global store of eight 32-bit words (32-byte aligned address).
+MXQ_DEV void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                          uint32_t a5, uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0),
+               "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
 MXQ_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 MXQ_DEV uint32_t cluster_rank() {
@@ -240,7 +250,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G_STAGES * G_STAGE_BYTES);
   uint64_t* empty = full + G_STAGES;
-  uint64_t* tmem_full = empty + G_STAGES;
+  uint64_t* sf_ready = empty + G_STAGES;
+  uint64_t* tmem_full = sf_ready + G_STAGES;
   uint64_t* tmem_empty = tmem_full + 1;      // leader: both CTAs drained the accumulator
   uint64_t* drain = tmem_empty + 1;
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -257,6 +268,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     for (int s = 0; s < G_STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);    // leader: one arrival, bytes of both CTAs
       mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&sf_ready[s]), 1);
     }
     mbar_init(smem_u32(tmem_full), 1);
     mbar_init(smem_u32(tmem_empty), 8 * G_CLUSTER);
@@ -347,37 +359,25 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         }
         tc_fence_after();
         for (int ks = 0; ks < nk; ++ks) {
-          if (!mbar_try_wait_cluster(smem_u32(&full[s]), phase) &&
-              !gwait(smem_u32(&full[s]), phase, tmo, abort_flag)) {
+          if (!mbar_try_wait_cluster(smem_u32(&sf_ready[s]), phase) &&
+              !gwait(smem_u32(&sf_ready[s]), phase, tmo, abort_flag)) {
             if (!*abort_flag) gabort(abort_flag, SITE_GEMM_FULL);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sfa_smem = st0 + s * G_STAGE_BYTES + G_A_BYTES + G_B_BYTES;
-          const uint32_t sfb_smem = sfa_smem + G_SFA_BYTES;
           const uint32_t sfa_t = tmem + G_SFA_COL0 + 8 * s;
           const uint32_t sfb_t = tmem + G_SFB_COL0 + 16 * s;
           const uint64_t ad = adesc_s0 + s * kStageDesc;
           const uint64_t bd = bdesc_s0 + s * kStageDesc;
-          // scales -> tensor memory of both CTAs.  A (own rows): chunk c ->
-          // columns +4c.  B: k-chunk c of rows 0-127 -> +8c, rows 128-255 -> +8c+4.
+          // scales of this stage are already in tensor memory (sf_ready)
           if (fp4) {
-            tc_cp_sf_pair(sfa_t, sfa_smem);
-            tc_cp_sf_pair(sfa_t + 4, sfa_smem + 512);
-            tc_cp_sf_pair(sfb_t, sfb_smem);
-            tc_cp_sf_pair(sfb_t + 8, sfb_smem + 512);
-            tc_cp_sf_pair(sfb_t + 4, sfb_smem + 1024);
-            tc_cp_sf_pair(sfb_t + 12, sfb_smem + 1536);
             // each MMA consumes 32 bytes of K (K=64 packed E2M1), k-blocks 2j, 2j+1
             mma_mxf4_pair(tmem, ad, bd, idesc[0], sfa_t, sfb_t, ks > 0 ? 1u : 0u);
             mma_mxf4_pair(tmem, ad + 2, bd + 2, idesc[1], sfa_t, sfb_t, 1u);
             mma_mxf4_pair(tmem, ad + 4, bd + 4, idesc[2], sfa_t + 4, sfb_t + 8, 1u);
             mma_mxf4_pair(tmem, ad + 6, bd + 6, idesc[3], sfa_t + 4, sfb_t + 8, 1u);
           } else {
-            tc_cp_sf_pair(sfa_t, sfa_smem);
-            tc_cp_sf_pair(sfb_t, sfb_smem);
-            tc_cp_sf_pair(sfb_t + 4, sfb_smem + 512);
             // each MMA consumes 32 bytes of K (K=32 E4M3), k-block j
             mma_mxf8_pair(tmem, ad, bd, idesc[0], sfa_t, sfb_t, ks > 0 ? 1u : 0u);
             mma_mxf8_pair(tmem, ad + 2, bd + 2, idesc[1], sfa_t, sfb_t, 1u);
@@ -394,6 +394,44 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       tc_commit_pair_mc(smem_u32(drain), 0x1);
       if (!mbar_wait(smem_u32(drain), 0, tmo))
         record_error(&g_err_gemm, MXQ_ERR_TIMEOUT, SITE_GEMM_DRAIN);
+    }
+  } else if (warp == 10) {
+    if (lane == 0 && leader) {
+      // ---------------- scale copier (leader CTA) ----------------
+      // Copies each stage's scales into both CTAs' tensor memory and signals
+      // the MMA lane through sf_ready; a separate thread, because every
+      // tcgen05 instruction occupies its issuing thread for ~100 cycles.
+      const uint32_t st0 = smem_u32(smem);
+      const bool fp4 = a.fp4 != 0;
+      uint32_t s = 0, phase = 0;
+      const uint32_t n_my = n_tiles > cid ? (n_tiles - cid + ncl - 1) / ncl : 0;
+      const uint32_t total = n_my * nk;
+      for (uint32_t it = 0; it < total; ++it) {
+        if (!mbar_try_wait_cluster(smem_u32(&full[s]), phase) &&
+            !gwait(smem_u32(&full[s]), phase, tmo, abort_flag)) {
+          if (!*abort_flag) gabort(abort_flag, SITE_GEMM_FULL);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sfa_smem = st0 + s * G_STAGE_BYTES + G_A_BYTES + G_B_BYTES;
+        const uint32_t sfb_smem = sfa_smem + G_SFA_BYTES;
+        const uint32_t sfa_t = tmem + G_SFA_COL0 + 8 * s;
+        const uint32_t sfb_t = tmem + G_SFB_COL0 + 16 * s;
+        if (fp4) {
+          tc_cp_sf_pair(sfa_t, sfa_smem);
+          tc_cp_sf_pair(sfa_t + 4, sfa_smem + 512);
+          tc_cp_sf_pair(sfb_t, sfb_smem);
+          tc_cp_sf_pair(sfb_t + 8, sfb_smem + 512);
+          tc_cp_sf_pair(sfb_t + 4, sfb_smem + 1024);
+          tc_cp_sf_pair(sfb_t + 12, sfb_smem + 1536);
+        } else {
+          tc_cp_sf_pair(sfa_t, sfa_smem);
+          tc_cp_sf_pair(sfb_t, sfb_smem);
+          tc_cp_sf_pair(sfb_t + 4, sfb_smem + 512);
+        }
+        tc_commit_pair_mc(smem_u32(&sf_ready[s]), 0x1);
+        if (++s == G_STAGES) { s = 0; phase ^= 1; }
+      }
     }
   } else {
     // ---------------- epilogue (warps 2..9, both CTAs) ----------------
@@ -425,25 +463,39 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const int64_t ncols = (a.N - col0) < 128 ? (a.N - col0) : 128;
         if (a.out_bf16) {
           __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(a.C) + row * a.N + col0;
+          uint32_t p[64];
 #pragma unroll
-          for (int c = 0; c < 128; c += 8) {
-            if (c < ncols) {
-              uint32_t p[4];
+          for (int u = 0; u < 64; ++u) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[2 * u]),
+                                                           __uint_as_float(v[2 * u + 1]));
+            p[u] = *reinterpret_cast<const uint32_t*>(&b);
+          }
+          if (a.wide_stores) {
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[c + 2 * u]),
-                                                               __uint_as_float(v[c + 2 * u + 1]));
-                p[u] = *reinterpret_cast<const uint32_t*>(&b);
-              }
-              *reinterpret_cast<uint4*>(crow + c) = make_uint4(p[0], p[1], p[2], p[3]);
-            }
+            for (int c = 0; c < 128; c += 16)
+              if (c < ncols)
+                st_global_v8(crow + c, p[c / 2], p[c / 2 + 1], p[c / 2 + 2], p[c / 2 + 3],
+                             p[c / 2 + 4], p[c / 2 + 5], p[c / 2 + 6], p[c / 2 + 7]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; c += 8)
+              if (c < ncols)
+                *reinterpret_cast<uint4*>(crow + c) =
+                    make_uint4(p[c / 2], p[c / 2 + 1], p[c / 2 + 2], p[c / 2 + 3]);
           }
         } else {
           float* crow = static_cast<float*>(a.C) + row * a.N + col0;
+          if (a.wide_stores) {
 #pragma unroll
-          for (int c = 0; c < 128; c += 4) {
-            if (c < ncols)
-              *reinterpret_cast<uint4*>(crow + c) = make_uint4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+            for (int c = 0; c < 128; c += 8)
+              if (c < ncols)
+                st_global_v8(crow + c, v[c], v[c + 1], v[c + 2], v[c + 3], v[c + 4], v[c + 5],
+                             v[c + 6], v[c + 7]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; c += 4)
+              if (c < ncols)
+                *reinterpret_cast<uint4*>(crow + c) = make_uint4(v[c], v[c + 1], v[c + 2], v[c + 3]);
           }
         }
       }
@@ -624,6 +676,8 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   a.C = C;
   a.out_bf16 = out_dtype == MXQ_OUT_BF16;
   a.fp4 = fmt == MXQ_E2M1;
+  a.wide_stores = (reinterpret_cast<uintptr_t>(C) & 31u) == 0 &&
+                  N % (out_dtype == MXQ_OUT_F32 ? 8 : 16) == 0;
   a.timeout_ns = wait_timeout_ns();
 
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(mx_gemm_kernel),
