@@ -21,8 +21,9 @@
 //              leader CTA one lane issues the four pair MMAs of each stage
 //              into the fp32 accumulators (each CTA: 128 lanes x 256
 //              columns), then releases the stage in both CTAs;
-//   warp 10    (leader) one lane copies each stage's scales into both CTAs'
-//              tensor memory (tcgen05.cp) ahead of the MMA lane;
+//   warps 10-11 (leader) one lane each copies part of each stage's scales
+//              into both CTAs' tensor memory (tcgen05.cp) ahead of the MMA
+//              lane;
 //   warps 2-9  (both CTAs) epilogue: each drains 32 accumulator lanes x 128
 //              columns into registers, tells the leader the accumulator is
 //              free, and stores its rows (256-bit stores when aligned) while
@@ -47,7 +48,7 @@ constexpr int G_BN = 256;                    // columns of the tile (rows of B)
 constexpr int G_BN_CTA = G_BN / G_CLUSTER;   // rows of B each CTA holds
 constexpr int G_BKB = 128;                   // bytes of K per stage (one 128 B swizzle row)
 constexpr int G_STAGES = 6;
-constexpr int G_THREADS = 352;               // 11 warps
+constexpr int G_THREADS = 384;               // 12 warps
 constexpr int G_A_BYTES = G_BM * G_BKB;      // 16 KB
 constexpr int G_B_BYTES = G_BN_CTA * G_BKB;  // 16 KB
 constexpr int G_SFA_BYTES = 1024;            // own 128 rows: up to 2 chunks of 512 B
@@ -64,6 +65,8 @@ static_assert(G_STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 struct GArgs {
   int32_t M, N;
   int32_t n_mp, n_nt, n_tiles;  // 256-row pair tiles along M, 256-col tiles along N
+  int32_t group;                // tiles per raster group along the grouped dimension
+  int32_t group_n;              // 1: groups run along N, 0: along M
   int32_t nk;                   // K stages
   int32_t kc_per_row;           // 512-byte scale chunks per 128-row tile (KBp / 4)
   const uint8_t* sfa;           // chunked scales of A in the workspace
@@ -241,6 +244,24 @@ MXQ_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar
       : "memory");
 }
 
+// Work item t -> (mp, nt).  Tiles are visited in groups of `group` rows (or
+// columns, when group_n): inside a group the grouped index runs fastest, so
+// the clusters working at one time cover `group` panels of one operand and a
+// few of the other, and the grouped operand's panels stay in L2 while the
+// group sweeps the other dimension.
+MXQ_DEV void tile_coords(int t, const GArgs& a, int& mp, int& nt) {
+  const int n_g = a.group_n ? a.n_nt : a.n_mp;   // grouped dimension
+  const int n_o = a.group_n ? a.n_mp : a.n_nt;   // swept dimension
+  const int per_group = a.group * n_o;
+  const int g = t / per_group;
+  const int first = g * a.group;
+  const int size = min(a.group, n_g - first);
+  const int local = t - g * per_group;
+  const int gi = first + local % size, oi = local / size;
+  mp = a.group_n ? oi : gi;
+  nt = a.group_n ? gi : oi;
+}
+
 __global__ void __launch_bounds__(G_THREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -268,7 +289,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     for (int s = 0; s < G_STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);    // leader: one arrival, bytes of both CTAs
       mbar_init(smem_u32(&empty[s]), 1);
-      mbar_init(smem_u32(&sf_ready[s]), 1);
+      mbar_init(smem_u32(&sf_ready[s]), 2);  // two scale-copy warps
     }
     mbar_init(smem_u32(tmem_full), 1);
     mbar_init(smem_u32(tmem_empty), 8 * G_CLUSTER);
@@ -282,7 +303,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   tc_fence_after();
   const int cid = blockIdx.x / G_CLUSTER, ncl = gridDim.x / G_CLUSTER;
   const uint32_t tmem = *tmem_base_slot;
-  const int n_tiles = a.n_tiles, n_nt = a.n_nt, nk = a.nk;
+  const int n_tiles = a.n_tiles, nk = a.nk;
   const uint64_t tmo = a.timeout_ns;
 
   const int n_sfa = a.fp4 ? 2 : 1;            // 512-byte chunks of own-A scales per stage
@@ -298,7 +319,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       uint32_t s = 0, phase = 0, issued = 0;
       bool ok = true;
       for (int t = cid; t < n_tiles && ok; t += ncl) {
-        const int nt = t % n_nt, mp = t / n_nt;
+        int mp, nt;
+        tile_coords(t, a, mp, nt);
         const int mt = G_CLUSTER * mp + static_cast<int>(rank);   // this CTA's 128-row tile
         const int srow_a = mt * a.kc_per_row;                     // first scale chunk rows
         const int srow_b0 = (2 * nt) * a.kc_per_row, srow_b1 = (2 * nt + 1) * a.kc_per_row;
@@ -395,12 +417,15 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       if (!mbar_wait(smem_u32(drain), 0, tmo))
         record_error(&g_err_gemm, MXQ_ERR_TIMEOUT, SITE_GEMM_DRAIN);
     }
-  } else if (warp == 10) {
+  } else if (warp >= 10) {
     if (lane == 0 && leader) {
-      // ---------------- scale copier (leader CTA) ----------------
-      // Copies each stage's scales into both CTAs' tensor memory and signals
-      // the MMA lane through sf_ready; a separate thread, because every
-      // tcgen05 instruction occupies its issuing thread for ~100 cycles.
+      // ---------------- scale copiers (leader CTA, warps 10 and 11) -------
+      // Copy each stage's scales into both CTAs' tensor memory ahead of the
+      // MMA lane and signal it through sf_ready (two arrivals per stage).
+      // Separate threads, because every tcgen05 instruction occupies its
+      // issuing thread for ~100 cycles: warp 10 copies the A scales and the
+      // scales of B rows 0-127, warp 11 those of B rows 128-255.
+      const bool first = warp == 10;
       const uint32_t st0 = smem_u32(smem);
       const bool fp4 = a.fp4 != 0;
       uint32_t s = 0, phase = 0;
@@ -417,17 +442,18 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const uint32_t sfb_smem = sfa_smem + G_SFA_BYTES;
         const uint32_t sfa_t = tmem + G_SFA_COL0 + 8 * s;
         const uint32_t sfb_t = tmem + G_SFB_COL0 + 16 * s;
-        if (fp4) {
+        // A: chunk c -> columns +4c.  B: k-chunk c of rows 0-127 -> +8c,
+        // rows 128-255 -> +8c+4 (rows 128-255 start sf_bytes_a into the slot)
+        if (first) {
           tc_cp_sf_pair(sfa_t, sfa_smem);
-          tc_cp_sf_pair(sfa_t + 4, sfa_smem + 512);
           tc_cp_sf_pair(sfb_t, sfb_smem);
-          tc_cp_sf_pair(sfb_t + 8, sfb_smem + 512);
-          tc_cp_sf_pair(sfb_t + 4, sfb_smem + 1024);
-          tc_cp_sf_pair(sfb_t + 12, sfb_smem + 1536);
+          if (fp4) {
+            tc_cp_sf_pair(sfa_t + 4, sfa_smem + 512);
+            tc_cp_sf_pair(sfb_t + 8, sfb_smem + 512);
+          }
         } else {
-          tc_cp_sf_pair(sfa_t, sfa_smem);
-          tc_cp_sf_pair(sfb_t, sfb_smem);
-          tc_cp_sf_pair(sfb_t + 4, sfb_smem + 512);
+          tc_cp_sf_pair(sfb_t + 4, sfb_smem + sf_bytes_a);
+          if (fp4) tc_cp_sf_pair(sfb_t + 12, sfb_smem + sf_bytes_a + 512);
         }
         tc_commit_pair_mc(smem_u32(&sf_ready[s]), 0x1);
         if (++s == G_STAGES) { s = 0; phase ^= 1; }
@@ -456,7 +482,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(empty_leader);
 
-      const int nt = t % n_nt, mp = t / n_nt;
+      int mp, nt;
+      tile_coords(t, a, mp, nt);
       const int64_t row = (int64_t(mp) * G_CLUSTER + rank) * G_BM + quad * 32 + lane;
       const int64_t col0 = int64_t(nt) * G_BN + colh * 128;
       if (row < a.M && col0 < a.N) {
@@ -508,27 +535,35 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   if (warp == 1) tmem_dealloc_pair(tmem, G_TMEM_COLS);
 }
 
-// Row-major E8M0 scales [rows][kb] -> chunked tensor-core layout, zero padded
-// to rows_p rows and kbp blocks.  One thread writes the four blocks of one
-// row in one chunk.
+// Row-major E8M0 scales [rows][kb] of A and of B -> chunked tensor-core
+// layout, zero padded to rows_p rows and kbp blocks, both operands in one
+// launch.  One thread writes the four blocks of one row in one chunk.
+struct SfSide {
+  const uint8_t* s;
+  int64_t rows, rows_p;
+  uint8_t* out;
+};
+
 __global__ void __launch_bounds__(256)
-    sf_to_chunks(const uint8_t* __restrict__ s, int64_t rows, int64_t kb, int64_t rows_p,
-                 int64_t kbp, uint8_t* __restrict__ out) {
+    sf_to_chunks(SfSide sa, SfSide sb, int64_t kb, int64_t kbp) {
   const int64_t kcs = kbp / 4;
-  const int64_t total = rows_p * kcs;
+  const int64_t total_a = sa.rows_p * kcs, total = total_a + sb.rows_p * kcs;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = i % rows_p, kc = i / rows_p;
+    const bool is_a = i < total_a;
+    const SfSide& d = is_a ? sa : sb;
+    const int64_t j = is_a ? i : i - total_a;
+    const int64_t r = j % d.rows_p, kc = j / d.rows_p;
     uint32_t w = 0;
-    if (r < rows) {
+    if (r < d.rows) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t k = kc * 4 + u;
-        if (k < kb) w |= static_cast<uint32_t>(s[r * kb + k]) << (8 * u);
+        if (k < kb) w |= static_cast<uint32_t>(d.s[r * kb + k]) << (8 * u);
       }
     }
     const int64_t rt = r / 128, rr = r % 128;
-    uint8_t* chunk = out + (rt * kcs + kc) * 512;
+    uint8_t* chunk = d.out + (rt * kcs + kc) * 512;
     *reinterpret_cast<uint32_t*>(chunk + (rr % 32) * 16 + (rr / 32) * 4) = w;
   }
 }
@@ -612,11 +647,10 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   {
-    const int64_t ta = p.mp * (p.kbp / 4), tb = p.np * (p.kbp / 4);
-    const int ga = static_cast<int>(std::min<int64_t>((ta + 255) / 256, 4 * sm_count()));
-    const int gb = static_cast<int>(std::min<int64_t>((tb + 255) / 256, 4 * sm_count()));
-    sf_to_chunks<<<ga, 256, 0, st>>>(sA, M, p.kb, p.mp, p.kbp, ws);
-    sf_to_chunks<<<gb, 256, 0, st>>>(sB, N, p.kb, p.np, p.kbp, ws + p.ws_a);
+    const int64_t total = (p.mp + p.np) * (p.kbp / 4);
+    const int grid = static_cast<int>(std::min<int64_t>((total + 255) / 256, 4 * sm_count()));
+    const SfSide sa{sA, M, p.mp, ws}, sb{sB, N, p.np, ws + p.ws_a};
+    sf_to_chunks<<<grid, 256, 0, st>>>(sa, sb, p.kb, p.kbp);
   }
 
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
@@ -661,7 +695,7 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
     }
   }
 
-  GArgs a;
+  GArgs a{};
   a.M = static_cast<int32_t>(M);
   a.N = static_cast<int32_t>(N);
   a.n_mp = static_cast<int32_t>(p.mp / (G_CLUSTER * G_BM));
@@ -669,6 +703,31 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   // one work item = one 256x256 pair tile (one cluster)
   if (int64_t(a.n_mp) * a.n_nt >= (int64_t(1) << 31)) return MXQ_ERR_ARG;
   a.n_tiles = a.n_mp * a.n_nt;
+  {
+    // Raster: tiles run in groups of `group` panels of one operand (the
+    // grouped one) while the group sweeps all panels of the other.  The
+    // grouped panels are touched by every wave of the group and stay in L2
+    // (budget 40 MB); the swept operand streams from DRAM once per group.
+    // Modeled DRAM bytes: grouped_total + swept_total * n_groups; the
+    // orientation and group size with the fewest bytes win.
+    const double l2_budget = 40.0 * (1 << 20);
+    const double panel = double(2 * G_BM) * double(p.kbytes);
+    const int g_fit = static_cast<int>(std::max(1.0, std::floor(l2_budget / panel)));
+    const double a_bytes = double(p.mp) * p.kbytes, b_bytes = double(p.np) * p.kbytes;
+    double best = -1.0;
+    for (int orient = 0; orient < 2; ++orient) {
+      const int n_g = orient ? a.n_nt : a.n_mp;
+      const double grouped = orient ? b_bytes : a_bytes, swept = orient ? a_bytes : b_bytes;
+      for (int g = 1; g <= std::min(g_fit, n_g); ++g) {
+        const double bytes = grouped + swept * std::ceil(double(n_g) / g);
+        if (best < 0.0 || bytes < best - 1.0) {
+          best = bytes;
+          a.group_n = orient;
+          a.group = g;
+        }
+      }
+    }
+  }
   a.nk = static_cast<int32_t>((p.kbytes + G_BKB - 1) / G_BKB);
   a.kc_per_row = static_cast<int32_t>(p.kbp / 4);
   a.sfa = ws;
@@ -679,6 +738,10 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   a.wide_stores = (reinterpret_cast<uintptr_t>(C) & 31u) == 0 &&
                   N % (out_dtype == MXQ_OUT_F32 ? 8 : 16) == 0;
   a.timeout_ns = wait_timeout_ns();
+  // every field the kernel dereferences or divides by is set
+  if (!a.C || !a.sfa || !a.sfb || a.nk <= 0 || a.kc_per_row <= 0 || a.group <= 0 ||
+      a.n_tiles <= 0 || a.n_nt <= 0 || a.n_mp <= 0)
+    return MXQ_ERR_ARG;
 
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(mx_gemm_kernel),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM) != cudaSuccess)
