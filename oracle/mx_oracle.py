@@ -28,11 +28,15 @@ specifications, restated here from their definitions:
   infinities; S.1111.111 is NaN; largest finite magnitude 1.75 * 2**8 = 448.
 * E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa bit; magnitudes
   {0, .5, 1, 1.5, 2, 3, 4, 6}; largest 6 = 1.5 * 2**2.
+* E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits, IEEE-style
+  specials: S.11111.00 is infinity, S.11111.xx (xx != 0) NaN; largest
+  finite magnitude 1.75 * 2**15 = 57344.  The other MXFP8 element type
+  ("Lumen：AMD原生大模型量化训练框架的技术突破与实践", §1 names FP8 E4M3 and E5M2).
 * E8M0 shared scale: an unsigned biased exponent, value 2**(s - 127); 0xFF
   is NaN.
 * The shared exponent of a block is floor(log2(amax)) - emax_elem, where
   emax_elem is the exponent of the element format's largest normal (8 for
-  E4M3, 2 for E2M1).  Elements are x / 2**e rounded to nearest, ties to
+  E4M3, 2 for E2M1, 15 for E5M2).  Elements are x / 2**e rounded to nearest, ties to
   even, clamped to the largest finite element magnitude.
 
 Readings taken where the sources are silent (each is also listed in the
@@ -41,8 +45,9 @@ design notes):
 R1  amax == 0 gives scale byte 0x00 (log2 0 = -inf, clamped to -127) and
     every element code +0 or -0.
 R2  a block holding NaN or +-Inf gets scale 0xFF and all element codes 0.
-R3  the exponent uses floor, so block maxima in (448, 512) or (6, 8) times
-    2**e saturate to the largest element.
+R3  the exponent uses floor, so block maxima in (448, 512), (6, 8) or
+    (57344, 65536) times 2**e saturate to the largest element (E5M2 elements
+    saturate too: they never become infinity).
 R4  signs are kept: a negative value that rounds to zero encodes as -0
     (0x80 for E4M3, 0x8 for E2M1).
 R5  E2M1 codes are packed two per byte, the even element in the low nibble.
@@ -71,11 +76,13 @@ BLOCK = 32  # MX block size ("MindSpeed LLM FSDP2量化特性", 第 1 步: MX-1-
 
 E4M3 = "e4m3"
 E2M1 = "e2m1"
+E5M2 = "e5m2"
 
 _FMT = {
     # ebits, mbits, bias, max finite magnitude, emax_elem, total bits
     E4M3: dict(ebits=4, mbits=3, bias=7, maxval=448.0, emax=8, bits=8),
     E2M1: dict(ebits=2, mbits=1, bias=1, maxval=6.0, emax=2, bits=4),
+    E5M2: dict(ebits=5, mbits=2, bias=15, maxval=57344.0, emax=15, bits=8),
 }
 
 
@@ -88,7 +95,8 @@ def decode_element(code: int, fmt: str) -> float:
 
     OCP MX v1.0 element types: normal (E > 0) is (1 + m / 2**mbits) *
     2**(E - bias); subnormal (E == 0) is m / 2**mbits * 2**(1 - bias).
-    E4M3 "fn": only S.1111.111 is NaN (no infinities).
+    E4M3 "fn": only S.1111.111 is NaN (no infinities).  E5M2: an all-ones
+    exponent is infinity (mantissa 0) or NaN (mantissa != 0).
     """
     p = _FMT[fmt]
     nb, mb = p["bits"], p["mbits"]
@@ -97,6 +105,8 @@ def decode_element(code: int, fmt: str) -> float:
     m = code & ((1 << mb) - 1)
     if fmt == E4M3 and E == 15 and m == 7:
         return float("nan")
+    if fmt == E5M2 and E == 31:
+        return float("nan") if m else (float("-inf") if sign else float("inf"))
     if E == 0:
         mag = (m / (1 << mb)) * 2.0 ** (1 - p["bias"])
     else:
@@ -105,7 +115,7 @@ def decode_element(code: int, fmt: str) -> float:
 
 
 def decode_table(fmt: str) -> np.ndarray:
-    """All code values of a format, index = code (256 for E4M3, 16 for E2M1)."""
+    """All code values of a format, index = code (256 for E4M3/E5M2, 16 for E2M1)."""
     n = 1 << _FMT[fmt]["bits"]
     return np.array([decode_element(c, fmt) for c in range(n)], dtype=np.float64)
 

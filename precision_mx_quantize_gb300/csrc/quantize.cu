@@ -60,13 +60,11 @@ template <>
 struct Elem<MXQ_E4M3> {
   static constexpr uint32_t emax = 8;  // 448 = 1.75 * 2^8
   static constexpr int words = 8;      // 32 one-byte codes
-  static constexpr int bytes = 32;
 };
 template <>
 struct Elem<MXQ_E2M1> {
   static constexpr uint32_t emax = 2;  // 6 = 1.5 * 2^2
   static constexpr int words = 4;      // 32 four-bit codes
-  static constexpr int bytes = 16;
 };
 
 // RN_fp32(2^-2.5) = RN_fp32(sqrt(2)) / 8: the normalization of H_32.

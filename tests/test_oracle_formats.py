@@ -51,7 +51,7 @@ def _brute_round(v, fmt):
     """Nearest finite code magnitude by exhaustive search; ties -> even code."""
     table = O.decode_table(fmt)
     n = len(table)
-    pos = [(c, table[c]) for c in range(n // 2) if not np.isnan(table[c])]
+    pos = [(c, table[c]) for c in range(n // 2) if np.isfinite(table[c])]
     mags = np.array([m for _, m in pos])
     codes = np.array([c for c, _ in pos])
     out = np.empty(len(v))
@@ -68,10 +68,10 @@ def _brute_round(v, fmt):
     return np.where(np.signbit(v), -out, out)
 
 
-@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M1])
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M1, O.E5M2])
 def test_rounding_brute_force(fmt):
     table = O.decode_table(fmt)
-    mags = np.unique(np.abs(table[~np.isnan(table)]))
+    mags = np.unique(np.abs(table[np.isfinite(table)]))
     mids = (mags[:-1] + mags[1:]) / 2
     f32 = np.float32
     cands = [mags, mids]
@@ -106,10 +106,10 @@ def test_e4m3_rounding_matches_torch_cast():
 
 
 def test_encode_decode_inverse():
-    for fmt in (O.E4M3, O.E2M1):
+    for fmt in (O.E4M3, O.E2M1, O.E5M2):
         t = O.decode_table(fmt)
         for c, val in enumerate(t):
-            if np.isnan(val):
+            if not np.isfinite(val):
                 continue
             assert O.encode_element(np.array([val]), fmt)[0] == c
 
@@ -131,7 +131,7 @@ def test_hand_derived_blocks(case):
 def _representable_block(rng, fmt, R, C):
     """Blocks whose values are element values times 2**e, amax in the top binade."""
     table = O.decode_table(fmt)
-    finite = table[~np.isnan(table)]
+    finite = table[np.isfinite(table)]
     vals = rng.choice(finite, size=(R, C))
     top = O.fmt_params(fmt)["maxval"]
     vals[:, ::32] = np.where(rng.random((R, C // 32)) < 0.5, top, -top)
@@ -139,7 +139,7 @@ def _representable_block(rng, fmt, R, C):
     return (vals.reshape(R, C // 32, 32) * np.exp2(e)[..., None]).reshape(R, C)
 
 
-@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M1])
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M1, O.E5M2])
 def test_exact_round_trip(fmt):
     rng = np.random.default_rng(5)
     z = _representable_block(rng, fmt, 8, 256).astype(np.float32)
@@ -151,7 +151,7 @@ def test_exact_round_trip(fmt):
         assert np.array_equal(back, z)
 
 
-@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M1])
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M1, O.E5M2])
 @pytest.mark.parametrize("k", [-20, -3, 1, 7, 30])
 def test_power_of_two_invariance(fmt, k):
     rng = np.random.default_rng(7)
@@ -190,7 +190,7 @@ def test_quantization_error_bound():
     # times the block's scale-normalised top value.
     rng = np.random.default_rng(3)
     x = rng.standard_normal((32, 256)).astype(np.float32)
-    for fmt in (O.E4M3, O.E2M1):
+    for fmt in (O.E4M3, O.E2M1, O.E5M2):
         c, s = O.mx_quantize(x, "row", fmt)
         back = O.dequantize_f64(c, s, fmt)
         scale = np.exp2(s.astype(np.float64) - 127)
@@ -201,3 +201,35 @@ def test_quantization_error_bound():
         bound = 2.0 ** (math.floor(math.log2(top)) - mb - 1)
         sat = (np.abs(x).reshape(32, 8, 32) / scale[..., None]) > top
         assert np.all(err[~sat] <= bound + 1e-12)
+
+
+def test_e5m2_decode_matches_torch_float8():
+    # torch's float8_e5m2 is an independent implementation of OCP FP8 E5M2
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e5m2).to(torch.float64).numpy()
+    ours = O.decode_table(O.E5M2)
+    assert np.array_equal(np.isnan(ref), np.isnan(ours))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], ours[ok])
+    assert np.array_equal(np.signbit(ref[ok]), np.signbit(ours[ok]))
+
+
+def test_e5m2_closed_forms():
+    t = O.decode_table(O.E5M2)
+    finite = t[np.isfinite(t)]
+    assert finite.max() == 57344.0 == 1.75 * 2 ** 15 == t[0x7B]
+    assert t[0x01] == 2.0 ** -16 and t[0x04] == 2.0 ** -14
+    assert np.isinf(t[0x7C]) and np.isinf(t[0xFC]) and t[0xFC] < 0
+    assert np.isnan(t).sum() == 6 and len(finite) == 248
+    assert O.fmt_params(O.E5M2)["emax"] == 15
+
+
+def test_e5m2_rounding_matches_torch_cast():
+    rng = np.random.default_rng(13)
+    v = np.concatenate([
+        rng.standard_normal(200_000) * np.exp2(rng.integers(-20, 16, 200_000)),
+        rng.uniform(-57344, 57344, 50_000),
+    ]).astype(np.float32)
+    v = v[np.abs(v) <= 57344]
+    ref = torch.from_numpy(v).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    ours = O.encode_element(O.round_to_element(v.astype(np.float64), O.E5M2), O.E5M2)
+    assert np.array_equal(ours, ref)
