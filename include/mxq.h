@@ -31,15 +31,17 @@
  *    argument errors are reported synchronously, device-side errors (a wait
  *    that timed out) by mxq_check().
  *  - Tensors are row-major.  A [rows, cols] bf16 tensor has row stride cols.
- *  - E4M3 codes take one byte per element.  E2M1 codes take half a byte:
- *    two per byte along the blocked axis, the even element in the low nibble.
+ *  - E4M3 and E5M2 codes take one byte per element.  E2M1 codes take half a
+ *    byte: two per byte along the blocked axis, the even element in the low
+ *    nibble.
  *  - E8M0 scale bytes: value 2^(s-127); 0xFF marks a block that held a NaN
  *    or an infinity (its codes are then all zero).  An all-zero block has
  *    scale 0x00.
  *  - Shared exponent e = floor(log2(amax)) - emax_elem (emax_elem = 8 for
- *    E4M3, 2 for E2M1), clamped to [-127, 127]; elements x * 2^-e are
- *    rounded to nearest, ties to even, saturating at 448 (E4M3) or 6 (E2M1);
- *    a negative value that rounds to zero keeps its sign.
+ *    E4M3, 15 for E5M2, 2 for E2M1), clamped to [-127, 127]; elements
+ *    x * 2^-e are rounded to nearest, ties to even, saturating at 448
+ *    (E4M3), 57344 (E5M2) or 6 (E2M1); a negative value that rounds to zero
+ *    keeps its sign.
  *  - Pointers to bf16 data and to codes must be 16-byte aligned; scales may
  *    have any alignment.
  *  - No call allocates device memory.
@@ -64,7 +66,10 @@ typedef enum {
   MXQ_ERR_WORKSPACE = 6     /* workspace too small                             */
 } mxq_status;
 
-typedef enum { MXQ_E4M3 = 0, MXQ_E2M1 = 1 } mxq_fmt;
+/* Element formats: E4M3 and E5M2 (MXFP8, one byte per element) and E2M1
+   (MXFP4, packed two per byte).  E5M2: [LUMEN] §1 names FP8 E5M2 beside
+   E4M3; OCP MX v1.0 lists it as the second MXFP8 element type. */
+typedef enum { MXQ_E4M3 = 0, MXQ_E2M1 = 1, MXQ_E5M2 = 2 } mxq_fmt;
 
 typedef enum {
   /* blocks of 32 run along cols; codes [rows][cols] (E2M1: [rows][cols/2]),
@@ -90,7 +95,8 @@ const char* mxq_status_str(int status);
  *   (block 32, E4M3).
  * layout: MXQ_ROWWISE needs cols % 32 == 0; MXQ_COLWISE_T needs
  *   rows % 32 == 0 and cols % 8 == 0.
- * fmt: MXQ_E4M3 or MXQ_E2M1.  codes / scales: outputs in the layout above.
+ * fmt: MXQ_E4M3, MXQ_E5M2 or MXQ_E2M1.  codes / scales: outputs in the
+ * layout above.
  * rows == 0 or cols == 0 is a no-op.  Dimensions must be < 2^31.
  */
 mxq_status mxq_quantize(const void* x, int64_t rows, int64_t cols, int layout, int fmt,
@@ -115,7 +121,9 @@ mxq_status mxq_hadamard_quantize(const void* x, int64_t rows, int64_t cols, int 
  * Hadamard if had_r != 0) and the column-wise transposed output (fmt_c,
  * Hadamard if had_c != 0).  The forward/dgrad operand and the Wgrad operand
  * of the same tensor ([AMD-FP4] §02) come from a single pass.
- * Needs rows % 32 == 0, cols % 32 == 0.  Outputs as in mxq_quantize.
+ * Needs rows % 32 == 0, cols % 32 == 0; fmt_r, fmt_c are MXQ_E4M3 or
+ * MXQ_E2M1 (MXQ_E5M2 returns MXQ_ERR_UNSUPPORTED here; use mxq_quantize).
+ * Outputs as in mxq_quantize.
  */
 mxq_status mxq_quantize_dual(const void* x, int64_t rows, int64_t cols,
                              int fmt_r, int had_r, void* codes_r, uint8_t* scales_r,
@@ -141,7 +149,7 @@ mxq_status mxq_dequantize(const void* codes, const uint8_t* scales, int64_t rows
  * A: codes [M][K] (E2M1: [M][K/2]), sA [M][K/32]; B: codes [N][K]
  * (E2M1: [N][K/2]), sB [N][K/32] -- both "K-major", as MXQ_ROWWISE (or
  * MXQ_COLWISE_T for the transposed operand) writes them.  Both operands use
- * the same fmt.  C: [M][N] row-major, fp32 or bf16 (out_dtype).
+ * the same fmt (MXQ_E4M3, MXQ_E5M2 or MXQ_E2M1).  C: [M][N] row-major, fp32 or bf16 (out_dtype).
  * K % 32 == 0, M >= 1, N >= 1; N % 4 == 0 (fp32) / N % 8 == 0 (bf16).
  * workspace: device scratch of at least mxq_gemm_workspace_size() bytes,
  * 256-byte aligned; it receives the scales in the tensor-core layout.

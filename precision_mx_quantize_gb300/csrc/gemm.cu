@@ -74,6 +74,7 @@ struct GArgs {
   void* C;
   int32_t out_bf16;
   int32_t fp4;
+  int32_t elem_code;            // A/B element type field of the instruction descriptor
   int32_t wide_stores;          // rows of C are 32-byte aligned: 256-bit stores
   uint64_t timeout_ns;
 };
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       // Everything that does not change per stage is computed once: each
       // tcgen05 instruction costs the issuing thread ~100 cycles, so the
       // loop keeps nothing else on its path.
-      const uint32_t fmt_code = a.fp4 ? 1u : 0u;  // kind::mxf4 E2M1 = 1, kind::mxf8f6f4 E4M3 = 0
+      const uint32_t fmt_code = static_cast<uint32_t>(a.elem_code);
       uint32_t idesc[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -575,10 +576,10 @@ struct Plan {
 
 bool make_plan(int64_t M, int64_t N, int64_t K, int fmt, Plan& p) {
   if (M <= 0 || N <= 0 || K <= 0 || K % 32 != 0) return false;
-  if (fmt != MXQ_E4M3 && fmt != MXQ_E2M1) return false;
-  p.kbytes = fmt == MXQ_E4M3 ? K : K / 2;
+  if (fmt != MXQ_E4M3 && fmt != MXQ_E2M1 && fmt != MXQ_E5M2) return false;
+  p.kbytes = fmt != MXQ_E2M1 ? K : K / 2;
   p.kb = K / 32;
-  p.skb = fmt == MXQ_E4M3 ? 4 : 8;  // k-blocks per 128-byte stage
+  p.skb = fmt != MXQ_E2M1 ? 4 : 8;  // k-blocks per 128-byte stage
   p.kbp = (p.kb + p.skb - 1) / p.skb * p.skb;
   p.mp = (M + G_CLUSTER * G_BM - 1) / (G_CLUSTER * G_BM) * (G_CLUSTER * G_BM);
   p.np = (N + G_BN - 1) / G_BN * G_BN;
@@ -735,6 +736,8 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   a.C = C;
   a.out_bf16 = out_dtype == MXQ_OUT_BF16;
   a.fp4 = fmt == MXQ_E2M1;
+  // kind::mxf8f6f4 element types: E4M3 = 0, E5M2 = 1; kind::mxf4: E2M1 = 1
+  a.elem_code = fmt == MXQ_E4M3 ? 0 : 1;
   a.wide_stores = (reinterpret_cast<uintptr_t>(C) & 31u) == 0 &&
                   N % (out_dtype == MXQ_OUT_F32 ? 8 : 16) == 0;
   a.timeout_ns = wait_timeout_ns();

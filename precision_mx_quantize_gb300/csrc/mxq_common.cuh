@@ -126,6 +126,19 @@ MXQ_DEV uint32_t cvt_e4m3x4(float a0, float a1, float a2, float a3) {
   return r;
 }
 
+// Four fp32 values -> four E5M2 codes (round to nearest even, saturating to
+// the largest finite magnitude), a0 in the lowest byte.
+MXQ_DEV uint32_t cvt_e5m2x4(float a0, float a1, float a2, float a3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return r;
+}
+
 // Eight fp32 values -> eight E2M1 codes packed in a word, a0 in the lowest
 // nibble.
 MXQ_DEV uint32_t cvt_e2m1x8(float a0, float a1, float a2, float a3, float a4, float a5, float a6,

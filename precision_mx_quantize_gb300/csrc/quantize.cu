@@ -62,6 +62,11 @@ struct Elem<MXQ_E4M3> {
   static constexpr int words = 8;      // 32 one-byte codes
 };
 template <>
+struct Elem<MXQ_E5M2> {
+  static constexpr uint32_t emax = 15;  // 57344 = 1.75 * 2^15
+  static constexpr int words = 8;       // 32 one-byte codes
+};
+template <>
 struct Elem<MXQ_E2M1> {
   static constexpr uint32_t emax = 2;  // 6 = 1.5 * 2^2
   static constexpr int words = 4;      // 32 four-bit codes
@@ -184,6 +189,12 @@ MXQ_DEV void quant_pair(float2 (&v)[32], uint32_t abA, uint32_t abB,
       oA[k] = cvt_e4m3x4(v[4 * k].x, v[4 * k + 1].x, v[4 * k + 2].x, v[4 * k + 3].x);
       oB[k] = cvt_e4m3x4(v[4 * k].y, v[4 * k + 1].y, v[4 * k + 2].y, v[4 * k + 3].y);
     }
+  } else if constexpr (FMT == MXQ_E5M2) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      oA[k] = cvt_e5m2x4(v[4 * k].x, v[4 * k + 1].x, v[4 * k + 2].x, v[4 * k + 3].x);
+      oB[k] = cvt_e5m2x4(v[4 * k].y, v[4 * k + 1].y, v[4 * k + 2].y, v[4 * k + 3].y);
+    }
   } else {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -208,11 +219,11 @@ MXQ_DEV int swz128(int r, int b) { return r * 128 + ((((b >> 4) ^ (r & 7)) << 4)
 // Byte offset of (row r, byte b of its 64-byte row) in a 64B-swizzled tile.
 MXQ_DEV int swz64(int r, int b) { return r * 64 + (((((b >> 4) ^ (r >> 1)) & 3) << 4) | (b & 15)); }
 
-// Write one block's codes into a staging tile whose rows are 128 B (E4M3,
-// 128B swizzle) or 64 B (E2M1, 64B swizzle).
+// Write one block's codes into a staging tile whose rows are 128 B (one-byte
+// codes, 128B swizzle) or 64 B (E2M1, 64B swizzle).
 template <int FMT>
 MXQ_DEV void stage_block(uint8_t* tile, int row, int block, const uint32_t (&o)[Elem<FMT>::words]) {
-  if constexpr (FMT == MXQ_E4M3) {
+  if constexpr (FMT != MXQ_E2M1) {
     *reinterpret_cast<uint4*>(tile + swz128(row, 32 * block)) = make_uint4(o[0], o[1], o[2], o[3]);
     *reinterpret_cast<uint4*>(tile + swz128(row, 32 * block + 16)) = make_uint4(o[4], o[5], o[6], o[7]);
   } else {
@@ -375,10 +386,10 @@ __global__ void __launch_bounds__(Q_THREADS, 2)
     __syncthreads();  // staging complete; stage s fully read
     if (tid == 0) {
       if constexpr (ROW)
-        tma_store_2d(&tm_r, smem_u32(out_r), static_cast<int32_t>(FR == MXQ_E4M3 ? C0 : C0 / 2),
+        tma_store_2d(&tm_r, smem_u32(out_r), static_cast<int32_t>(FR != MXQ_E2M1 ? C0 : C0 / 2),
                      static_cast<int32_t>(R0));
       if constexpr (COL)
-        tma_store_2d(&tm_c, smem_u32(out_c), static_cast<int32_t>(FC == MXQ_E4M3 ? R0 : R0 / 2),
+        tma_store_2d(&tm_c, smem_u32(out_c), static_cast<int32_t>(FC != MXQ_E2M1 ? R0 : R0 / 2),
                      static_cast<int32_t>(C0));
       bulk_commit();
       const int tn = t + Q_STAGES * gridDim.x;
@@ -427,6 +438,15 @@ MXQ_DEV float2 e4m3x2_to_f32(uint32_t two_codes) {
   return __half22float2(h);
 }
 
+MXQ_DEV float2 e5m2x2_to_f32(uint32_t two_codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e5m2x2 %0, c;\n\t}"
+      : "=r"(h2)
+      : "r"(two_codes));
+  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
+  return __half22float2(h);
+}
+
 MXQ_DEV float2 e2m1x2_to_f32(uint32_t byte) {
   uint32_t h2;
   asm("{\n\t.reg .b8 c;\n\t.reg .b16 w;\n\tcvt.u16.u32 w, %1;\n\tmov.b16 {c, _}, w;\n\t"
@@ -441,13 +461,13 @@ MXQ_DEV float2 e2m1x2_to_f32(uint32_t byte) {
 // row-wise code array (the 16 share one block and one scale).
 template <int FMT>
 MXQ_DEV void decode16(const uint8_t* codes, int64_t e0, float scale, float (&f)[16]) {
-  if constexpr (FMT == MXQ_E4M3) {
+  if constexpr (FMT != MXQ_E2M1) {
     const uint4 w = *reinterpret_cast<const uint4*>(codes + e0);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float2 lo = e4m3x2_to_f32(ws[i] & 0xFFFFu);
-      const float2 hi = e4m3x2_to_f32(ws[i] >> 16);
+      const float2 lo = FMT == MXQ_E4M3 ? e4m3x2_to_f32(ws[i] & 0xFFFFu) : e5m2x2_to_f32(ws[i] & 0xFFFFu);
+      const float2 hi = FMT == MXQ_E4M3 ? e4m3x2_to_f32(ws[i] >> 16) : e5m2x2_to_f32(ws[i] >> 16);
       f[4 * i] = lo.x * scale; f[4 * i + 1] = lo.y * scale;
       f[4 * i + 2] = hi.x * scale; f[4 * i + 3] = hi.y * scale;
     }
@@ -511,7 +531,7 @@ __global__ void __launch_bounds__(128) mx_dequant_cols(const uint8_t* __restrict
   const int cc = tid & 31, b = tid >> 5;
   const int64_t c = c0 + cc, rr = r0 + 32 * b;
   if (c < C && rr < R) {
-    const int64_t col_bytes = FMT == MXQ_E4M3 ? R : R / 2;
+    const int64_t col_bytes = FMT != MXQ_E2M1 ? R : R / 2;
     const float sc = scale_value(scales[c * (R >> 5) + (rr >> 5)]);
     const uint8_t* src = codes + c * col_bytes;
     float f[16];
@@ -550,11 +570,13 @@ QuantKernel kernel_ptr() {
 QuantKernel pick(bool row, bool col, int fr, int hr, int fc, int hc) {
 #define MXQ_K(R_, C_, FR_, HR_, FC_, HC_) kernel_ptr<R_, C_, FR_, HR_, FC_, HC_>()
   if (row && !col) {
-    if (fr == 0) return hr ? MXQ_K(true, false, 0, true, 0, false) : MXQ_K(true, false, 0, false, 0, false);
+    if (fr == MXQ_E4M3) return hr ? MXQ_K(true, false, 0, true, 0, false) : MXQ_K(true, false, 0, false, 0, false);
+    if (fr == MXQ_E5M2) return hr ? MXQ_K(true, false, 2, true, 0, false) : MXQ_K(true, false, 2, false, 0, false);
     return hr ? MXQ_K(true, false, 1, true, 0, false) : MXQ_K(true, false, 1, false, 0, false);
   }
   if (col && !row) {
-    if (fc == 0) return hc ? MXQ_K(false, true, 0, false, 0, true) : MXQ_K(false, true, 0, false, 0, false);
+    if (fc == MXQ_E4M3) return hc ? MXQ_K(false, true, 0, false, 0, true) : MXQ_K(false, true, 0, false, 0, false);
+    if (fc == MXQ_E5M2) return hc ? MXQ_K(false, true, 0, false, 2, true) : MXQ_K(false, true, 0, false, 2, false);
     return hc ? MXQ_K(false, true, 0, false, 1, true) : MXQ_K(false, true, 0, false, 1, false);
   }
 #define MXQ_DUAL_FC(FR_, HR_)                                                     \
@@ -568,7 +590,7 @@ QuantKernel pick(bool row, bool col, int fr, int hr, int fc, int hc) {
 #undef MXQ_K
 }
 
-bool valid_fmt(int f) { return f == MXQ_E4M3 || f == MXQ_E2M1; }
+bool valid_fmt(int f) { return f == MXQ_E4M3 || f == MXQ_E2M1 || f == MXQ_E5M2; }
 
 mxq_status quant_launch(const void* x, int64_t R, int64_t C, bool row, bool col, int fr, int hr,
                         void* codes_r, uint8_t* scales_r, int fc, int hc, void* codes_c,
@@ -602,13 +624,13 @@ mxq_status quant_launch(const void* x, int64_t R, int64_t C, bool row, bool col,
   // 64-byte swizzle, matching the staging layout in the kernel.
   auto code_map = [&](CUtensorMap* m, void* base, int64_t lines, int64_t line_elems,
                       int fmt) -> CUresult {
-    const int64_t lb = fmt == MXQ_E4M3 ? line_elems : line_elems / 2;
+    const int64_t lb = fmt != MXQ_E2M1 ? line_elems : line_elems / 2;
     const cuuint64_t d[2] = {static_cast<cuuint64_t>(lb), static_cast<cuuint64_t>(lines)};
     const cuuint64_t st[1] = {static_cast<cuuint64_t>(lb)};
-    const cuuint32_t bx[2] = {fmt == MXQ_E4M3 ? 128u : 64u, static_cast<cuuint32_t>(Q_ROWS)};
+    const cuuint32_t bx[2] = {fmt != MXQ_E2M1 ? 128u : 64u, static_cast<cuuint32_t>(Q_ROWS)};
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, d, st, bx, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  fmt == MXQ_E4M3 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  fmt != MXQ_E2M1 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   };
   CUtensorMap map_r, map_c;
@@ -674,6 +696,7 @@ extern "C" mxq_status mxq_quantize_dual(const void* x, int64_t rows, int64_t col
                                         int had_c, void* codes_c, uint8_t* scales_c,
                                         void* stream) {
   if (rows % 32 != 0 || cols % 32 != 0) return MXQ_ERR_ARG;
+  if (fmt_r == MXQ_E5M2 || fmt_c == MXQ_E5M2) return MXQ_ERR_UNSUPPORTED;
   return quant_launch(x, rows, cols, true, true, fmt_r, had_r != 0, codes_r, scales_r, fmt_c,
                       had_c != 0, codes_c, scales_c, stream);
 }
@@ -698,6 +721,9 @@ extern "C" mxq_status mxq_dequantize(const void* codes, const uint8_t* scales, i
     if (fmt == MXQ_E4M3) {
       if (bf) mx_dequant_rows<MXQ_E4M3, true><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
       else mx_dequant_rows<MXQ_E4M3, false><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
+    } else if (fmt == MXQ_E5M2) {
+      if (bf) mx_dequant_rows<MXQ_E5M2, true><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
+      else mx_dequant_rows<MXQ_E5M2, false><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
     } else {
       if (bf) mx_dequant_rows<MXQ_E2M1, true><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
       else mx_dequant_rows<MXQ_E2M1, false><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
@@ -710,6 +736,9 @@ extern "C" mxq_status mxq_dequantize(const void* codes, const uint8_t* scales, i
     if (fmt == MXQ_E4M3) {
       if (bf) mx_dequant_cols<MXQ_E4M3, true><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
       else mx_dequant_cols<MXQ_E4M3, false><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
+    } else if (fmt == MXQ_E5M2) {
+      if (bf) mx_dequant_cols<MXQ_E5M2, true><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
+      else mx_dequant_cols<MXQ_E5M2, false><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
     } else {
       if (bf) mx_dequant_cols<MXQ_E2M1, true><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
       else mx_dequant_cols<MXQ_E2M1, false><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);

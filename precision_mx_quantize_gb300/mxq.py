@@ -21,10 +21,10 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libmxq.so")
 
-E4M3, E2M1 = 0, 1
+E4M3, E2M1, E5M2 = 0, 1, 2
 ROWWISE, COLWISE_T = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
-FMTS = {"e4m3": E4M3, "e2m1": E2M1, E4M3: E4M3, E2M1: E2M1}
+FMTS = {"e4m3": E4M3, "e2m1": E2M1, "e5m2": E5M2, E4M3: E4M3, E2M1: E2M1, E5M2: E5M2}
 AXES = {"row": ROWWISE, "col": COLWISE_T, ROWWISE: ROWWISE, COLWISE_T: COLWISE_T}
 
 STATUS = {0: "MXQ_OK", 1: "MXQ_ERR_ARG", 2: "MXQ_ERR_ALIGN", 3: "MXQ_ERR_UNSUPPORTED",
@@ -141,7 +141,7 @@ def code_shape(rows: int, cols: int, axis, fmt):
     """(codes shape, scales shape) for a [rows, cols] tensor."""
     ax, f = AXES[axis], FMTS[fmt]
     r, c = (rows, cols) if ax == ROWWISE else (cols, rows)
-    return (r, c if f == E4M3 else c // 2), (r, c // 32)
+    return (r, c // 2 if f == E2M1 else c), (r, c // 32)
 
 
 def _alloc_codes(x, axis, fmt):

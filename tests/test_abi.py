@@ -51,3 +51,6 @@ def test_argument_errors_return_before_device_work(lib):
     assert mxq.mxq_hadamard_quantize(p, -32, 64, ROW, E2, p, p, None) == 1
     assert mxq.mxq_dequantize(p, p, 64, 48, ROW, E4, p, 0, None) == 1
     assert mxq.mxq_dequantize(p, p, 64, 64, ROW, E4, p, 3, None) == 1
+    # E5M2 is a single-layout format: the dual pass rejects it
+    assert mxq.mxq_quantize_dual(p, 64, 64, mxq.E5M2, 0, p, p, E2, 1, p, p, None) == 3
+    assert mxq.mxq_quantize(p, 64, 64, ROW, 3, p, p, None) == 1

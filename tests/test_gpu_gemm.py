@@ -68,7 +68,7 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1", "e5m2"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_gemm_small_full_compare(fmt, shape):
     M, N, K = shape
@@ -87,7 +87,7 @@ def test_gemm_bf16_output(fmt):
     _assert_close(got, ref, S, bf16=True)
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1", "e5m2"])
 def test_gemm_integer_exact(fmt):
     # small-integer elements with unit scales: fp32 accumulation is exact
     rng = np.random.default_rng(4)
@@ -105,14 +105,14 @@ def test_gemm_integer_exact(fmt):
     np.testing.assert_array_equal(got, ref.astype(np.float32))
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1", "e5m2"])
 def test_gemm_scale_placement(fmt):
     # one distinct scale per (row, k-block) for A and B, unit elements: every
     # output is a sum of distinct powers of two, so a scale read from the
     # wrong row or k-block changes the result
     rng = np.random.default_rng(5)
     M, N, K = 256, 512, 512
-    one = 0x38 if fmt == "e4m3" else 0x2
+    one = {"e4m3": 0x38, "e2m1": 0x2, "e5m2": 0x3C}[fmt]
     a = np.full((M, K), one, np.uint8)
     b = np.full((N, K), one, np.uint8)
     if fmt == "e2m1":

@@ -17,7 +17,7 @@ from tests.libutil import bf16_to_f32_np, ensure_built, to_np
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["e4m3", "e2m1"]
+FMTS = ["e4m3", "e2m1", "e5m2"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -149,6 +149,11 @@ def test_dequantize_arbitrary_scales():
     mxq.check()
     exp2 = O.mx_dequantize(c2.numpy(), s2.numpy(), "e2m1")
     np.testing.assert_array_equal(to_np(got2), exp2)
+    # E5M2: every code (its infinities and NaNs included) against every scale
+    got3 = mxq.mx_dequantize(codes.cuda(), scales.cuda(), 256, 256, "row", "e5m2")
+    mxq.check()
+    exp3 = O.mx_dequantize(codes.numpy(), scales.numpy(), "e5m2")
+    np.testing.assert_array_equal(to_np(got3), exp3)
 
 
 def test_small_round_trip_workload():
