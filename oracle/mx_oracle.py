@@ -60,6 +60,16 @@ R7  the Hadamard rotation is the natural-order (Sylvester) 32-point
     fp32 result without rounding it to bf16.
 R8  the GEMM is C[m, n] = sum_k dec(A[m, k]) * dec(B[n, k]) over the exactly
     dequantized operands (both K-major, "TN"), accumulated in fp64.
+R9  the ablation's random Hadamard rotation is H_32 * diag(d): one random
+    sign vector d (a 32-bit mask drawn by the caller) shared by every block
+    of the tensor, applied to the inputs before the fixed butterflies.
+R10 stochastic rounding rounds |v| up to the next grid point with
+    probability frac(|v| / q) (q the grid step at |v|), decided with 32
+    random bits per element: up iff bits < floor(frac * 2**32).  The block
+    exponent is the deterministic one (from the block amax).
+R11 the random bits of the element at input row r, column c come from
+    Philox4x32-10 keyed by the seed, counter (r * cols + c) // 4, word
+    (r * cols + c) % 4, for either output layout.
 
 Every function's citation is in its docstring.
 """
@@ -374,3 +384,121 @@ def mx_gemm_f64_rows(A, sA, B, sB, fmt: str, rows, cols):
     a = dequantize_f64(np.asarray(A)[rows], np.asarray(sA)[rows], fmt)
     b = dequantize_f64(np.asarray(B)[cols], np.asarray(sB)[cols], fmt)
     return a @ b.T, np.abs(a) @ np.abs(b).T
+
+
+# --------------------------------------------------------------------------
+# Ablation: random-sign Hadamard rotation and stochastic rounding
+# --------------------------------------------------------------------------
+# "AMD顛覆行業認知！終于攻克FP4大模型訓練致命難題", §01: the approaches the paper
+# argues against -- random Hadamard rotations and stochastic rounding, which
+# add randomness to the quantization error.  They are built here as an
+# ablation of the deterministic path.
+#
+# Random numbers come from Philox4x32-10 (Salmon, Moraes, Dror and Shaw,
+# "Parallel random numbers: as easy as 1, 2, 3", SC 2011), a counter-based
+# generator both sides implement from that definition.  The element at
+# linear index i of the input tensor (row-major, i = r * cols + c, whatever
+# the output layout) uses word i % 4 of Philox(counter = (i // 4 low 32 bits,
+# i // 4 high 32 bits, 0, 0), key = (seed low 32 bits, seed high 32 bits)).
+
+_PHILOX_M0, _PHILOX_M1 = 0xD2511F53, 0xCD9E8D57   # round multipliers
+_PHILOX_W0, _PHILOX_W1 = 0x9E3779B9, 0xBB67AE85   # key increments (golden ratio, sqrt(3)-1)
+
+
+def philox4x32_10(ctr, key):
+    """Philox4x32 with 10 rounds on arrays: ctr [..., 4], key [..., 2] (uint32)."""
+    c = [np.asarray(ctr[..., i], dtype=np.uint64) for i in range(4)]
+    k0 = np.asarray(key[..., 0], dtype=np.uint64)
+    k1 = np.asarray(key[..., 1], dtype=np.uint64)
+    mask = np.uint64(0xFFFFFFFF)
+    for rnd in range(10):
+        p0 = np.uint64(_PHILOX_M0) * c[0]        # exact 64-bit products of 32-bit words
+        p1 = np.uint64(_PHILOX_M1) * c[2]
+        hi0, lo0 = p0 >> np.uint64(32), p0 & mask
+        hi1, lo1 = p1 >> np.uint64(32), p1 & mask
+        c = [hi1 ^ c[1] ^ k0, lo1, hi0 ^ c[3] ^ k1, lo0]
+        if rnd < 9:
+            k0 = (k0 + np.uint64(_PHILOX_W0)) & mask
+            k1 = (k1 + np.uint64(_PHILOX_W1)) & mask
+    return np.stack([x.astype(np.uint32) for x in c], axis=-1)
+
+
+def element_random_bits(seed: int, index: np.ndarray) -> np.ndarray:
+    """32 random bits for each element linear index (see the rule above)."""
+    idx = np.asarray(index, dtype=np.uint64)
+    block = idx >> np.uint64(2)
+    ctr = np.zeros(idx.shape + (4,), dtype=np.uint32)
+    ctr[..., 0] = (block & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    ctr[..., 1] = (block >> np.uint64(32)).astype(np.uint32)
+    key = np.zeros(idx.shape + (2,), dtype=np.uint32)
+    key[..., 0] = np.uint32(seed & 0xFFFFFFFF)
+    key[..., 1] = np.uint32((seed >> 32) & 0xFFFFFFFF)
+    words = philox4x32_10(ctr, key)
+    return np.take_along_axis(words, (idx & np.uint64(3)).astype(np.int64)[..., None], axis=-1)[..., 0]
+
+
+def stochastic_round_to_element(v: np.ndarray, fmt: str, r: np.ndarray) -> np.ndarray:
+    """Round exact float64 values onto the element grid stochastically.
+
+    With lo <= |v| < hi the neighbouring grid points (step q, as in
+    round_to_element), F = floor(frac(|v| / q) * 2^32) and r the element's 32
+    random bits: the magnitude rounds up to hi when r < F, else down to lo,
+    so P(up) = (|v| - lo) / q up to 2^-32.  Values on the grid stay; the
+    result saturates at the largest finite magnitude; the sign is kept.
+    """
+    p = _FMT[fmt]
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    emin = 1 - p["bias"]
+    _, ex = np.frexp(a)
+    k = np.maximum(ex - 1, emin)
+    k = np.where(a == 0, emin, k)
+    step = np.ldexp(1.0, (k - p["mbits"]).astype(np.int64))
+    t = a / step                                   # exact power-of-two scaling
+    lo = np.floor(t)
+    F = np.floor((t - lo) * 2.0 ** 32)             # exact: the fraction has few bits
+    up = np.asarray(r, dtype=np.float64) < F
+    mag = np.where(up, lo + 1.0, lo) * step
+    mag = np.minimum(mag, p["maxval"])
+    return np.where(np.signbit(v), -mag, mag)
+
+
+def apply_sign_mask(blocks: np.ndarray, sign_mask: int) -> np.ndarray:
+    """Negate element i of every 32-block where bit i of sign_mask is set (exact)."""
+    b = np.asarray(blocks)
+    d = np.array([-1.0 if (sign_mask >> i) & 1 else 1.0 for i in range(BLOCK)], dtype=b.dtype)
+    return b * d
+
+
+def mx_quantize_ablation(x, axis: str, fmt: str, hadamard: bool, sign_mask: int,
+                         stochastic: bool, seed: int):
+    """MX quantization with the ablation's randomness.
+
+    hadamard: rotate each block by H_32 * diag(d), d_i = -1 where bit i of
+    sign_mask is set (a random diagonal drawn by the caller); sign_mask = 0 is
+    the deterministic rotation.  stochastic: element codes by
+    stochastic_round_to_element with Philox bits of each element's input
+    index; else round to nearest even.  The block exponent is chosen exactly
+    as in mx_quantize (from the rotated block's amax).
+    """
+    xf = np.asarray(x, dtype=np.float32)
+    R, C = xf.shape
+    idx = (np.arange(R, dtype=np.uint64)[:, None] * np.uint64(C)
+           + np.arange(C, dtype=np.uint64)[None, :])
+    src, sidx = (xf, idx) if axis == "row" else (xf.T, idx.T)
+    rows, cols = src.shape
+    blocks = src.reshape(rows, cols // BLOCK, BLOCK)
+    if hadamard:
+        blocks = fwht32(apply_sign_mask(blocks, sign_mask), np.float32)
+    s, e = shared_exponent(blocks, fmt)
+    v = np.ldexp(np.asarray(blocks, dtype=np.float64), -e[..., None])
+    if stochastic:
+        r = element_random_bits(seed, np.ascontiguousarray(sidx).reshape(rows, cols // BLOCK, BLOCK))
+        q = stochastic_round_to_element(v, fmt, r)
+    else:
+        q = round_to_element(v, fmt)
+    codes = encode_element(q, fmt)
+    codes = np.where((s == 255)[..., None], np.uint8(0), codes).reshape(rows, cols)
+    if fmt == E2M1:
+        codes = pack_e2m1(codes)
+    return np.ascontiguousarray(codes), np.ascontiguousarray(s)
