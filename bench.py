@@ -563,11 +563,33 @@ CASES = {
     "gemm-e2m1": ("gemm", (8192, 8192, 8192, "e2m1", "bf16")),
     "quant-dual-e4m3-he2m1": ("quant", (16384, 8192, "e4m3", False, "e2m1", True)),
     "quant-dual-he2m1-he2m1": ("quant", (16384, 8192, "e2m1", True, "e2m1", True)),
+    # ablation: column-wise random-sign Hadamard E2M1 with stochastic rounding
+    "ablate-col-rhe2m1-sr": ("ablate", (16384, 8192, "col", "e2m1", True, 0xA5A5F00F, True)),
+    "ablate-row-e4m3-sr": ("ablate", (16384, 8192, "row", "e4m3", False, 0, True)),
 }
 
 
-def run_case(name):
-    """Run one kernel case three times (for ncu captures of a single kernel)."""
+def _case_bytes(what, args):
+    """Algorithmic HBM bytes of one launch of a case (bf16 in, codes + scales out)."""
+    if what == "quant":
+        R, C, fr, _, fc, _ = args
+        out = sum(R * C * (0.5 if f == "e2m1" else 1.0) + R * C / 32 for f in (fr, fc))
+        return 2 * R * C + out
+    if what == "ablate":
+        R, C, _, f, _, _, _ = args
+        return 2 * R * C + R * C * (0.5 if f == "e2m1" else 1.0) + R * C / 32
+    M, N, K, fmt, od = args
+    eb = 1.0 if fmt == "e4m3" else 0.5
+    return (M + N) * K * (eb + 1 / 32) + M * N * (4 if od == "f32" else 2)
+
+
+def run_case(name, timed=False):
+    """Run one kernel case three times (for ncu captures of a single kernel).
+
+    timed: instead, time 20 launches after 5 warm-up launches with CUDA events
+    on the launching stream (inputs larger than L2) and print the average
+    launch time with the algorithmic GB/s or TFLOP/s against the peaks.
+    """
     import torch
 
     from precision_mx_quantize_gb300 import mxq
@@ -585,16 +607,45 @@ def run_case(name):
         dt = torch.float32 if od == "f32" else torch.bfloat16
         C = torch.empty((M, N), dtype=dt, device="cuda")
         ws = mxq.gemm_workspace(M, N, K, fmt, "cuda")
-        for _ in range(3):
-            mxq.mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=dt, out=C, workspace=ws)
-    else:
+        launch = lambda: mxq.mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=dt, out=C, workspace=ws)
+    elif what == "quant":
         R, Cc, fr, hr, fc, hc = args
         x = torch.randn(R, Cc, device="cuda", generator=g).to(torch.bfloat16)
         out = mxq.mx_quantize_dual(x, fr, hr, fc, hc)
-        for _ in range(2):
-            mxq.mx_quantize_dual(x, fr, hr, fc, hc, out=out)
+        launch = lambda: mxq.mx_quantize_dual(x, fr, hr, fc, hc, out=out)
+    else:
+        R, Cc, axis, f, had, mask, sr = args
+        x = torch.randn(R, Cc, device="cuda", generator=g).to(torch.bfloat16)
+        out = mxq.mx_quantize_ablation(x, axis, f, had, mask, sr, 1)
+        launch = lambda: mxq.mx_quantize_ablation(x, axis, f, had, mask, sr, 1, out=out)
+    if not timed:
+        for _ in range(3 if what == "gemm" else 2):
+            launch()
+        mxq.check()
+        print(json.dumps({"case": name, "status": "ok"}))
+        return
+    for _ in range(5):
+        launch()
+    torch.cuda.synchronize()
+    n = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        launch()
+    e1.record()
+    torch.cuda.synchronize()
     mxq.check()
-    print(json.dumps({"case": name, "status": "ok"}))
+    ms = e0.elapsed_time(e1) / n
+    peaks = _peaks()
+    line = {"case": name, "ms_per_launch": round(ms, 4)}
+    if what == "gemm":
+        M, N, K, fmt, _ = args
+        tf = 2 * M * N * K / ms / 1e9
+        line.update({"TFLOP/s": round(tf, 1)})
+    gbs = _case_bytes(what, args) / ms / 1e6
+    line.update({"algorithmic_GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3),
+                 "peak_source": peaks["source"]})
+    print(json.dumps(line))
 
 
 def main():
@@ -607,9 +658,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--case", choices=sorted(CASES), help="run one kernel case (for ncu) and exit")
+    ap.add_argument("--timed", action="store_true", help="with --case: time the case's launches")
     args = ap.parse_args()
     if args.case:
-        run_case(args.case)
+        run_case(args.case, timed=args.timed)
         return
     args.warmup = max(3, args.warmup)
 

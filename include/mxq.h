@@ -131,6 +131,34 @@ mxq_status mxq_quantize_dual(const void* x, int64_t rows, int64_t cols,
                              void* stream);
 
 /*
+ * Ablation quantizer: MX quantization with the randomness that [AMD-FP4] §01
+ * sets against its deterministic rotation -- a random Hadamard rotation and
+ * stochastic rounding.  Single layout, arguments and preconditions as
+ * mxq_quantize, plus:
+ *   hadamard   != 0: rotate every block by H_32 * diag(d) before quantizing,
+ *              d_i = -1 where bit i of sign_mask is set, else +1 (one random
+ *              sign vector drawn by the caller, shared by all blocks; the
+ *              butterflies and the normalization are those of
+ *              mxq_hadamard_quantize).  sign_mask must be 0 when hadamard
+ *              is 0 (MXQ_ERR_ARG otherwise).
+ *   stochastic != 0: element codes by stochastic rounding instead of round
+ *              to nearest even.  With q the element grid step at |v| (v the
+ *              element divided by the block scale), |v| rounds up to the next
+ *              grid point iff bits < floor(frac(|v| / q) * 2^32), where bits
+ *              is word (i % 4) of Philox4x32-10(counter = (i / 4 low 32 bits,
+ *              i / 4 high 32 bits, 0, 0), key = (seed low 32, seed high 32))
+ *              and i = input row * cols + input column (the same bits for
+ *              either layout).  Saturates at the largest finite element; the
+ *              sign is kept.  The block exponent is the deterministic one.
+ * hadamard == 0 and stochastic == 0 is mxq_quantize; sign_mask == 0 without
+ * stochastic rounding is mxq_hadamard_quantize.  The output depends only on
+ * x, sign_mask and seed.
+ */
+mxq_status mxq_quantize_ablation(const void* x, int64_t rows, int64_t cols, int layout, int fmt,
+                                 int hadamard, uint32_t sign_mask, int stochastic, uint64_t seed,
+                                 void* codes, uint8_t* scales, void* stream);
+
+/*
  * Dequantization: out[r][c] = dec(code) * 2^(s-127), exact in fp32 (an
  * overflow gives inf; scale 0xFF gives NaN); bf16 output is that fp32 value
  * rounded to nearest even.  OCP MX v1.0 (value of an MX element).

@@ -471,7 +471,8 @@ def apply_sign_mask(blocks: np.ndarray, sign_mask: int) -> np.ndarray:
 
 
 def mx_quantize_ablation(x, axis: str, fmt: str, hadamard: bool, sign_mask: int,
-                         stochastic: bool, seed: int):
+                         stochastic: bool, seed: int, first_row: int = 0, first_col: int = 0,
+                         total_cols=None):
     """MX quantization with the ablation's randomness.
 
     hadamard: rotate each block by H_32 * diag(d), d_i = -1 where bit i of
@@ -480,11 +481,17 @@ def mx_quantize_ablation(x, axis: str, fmt: str, hadamard: bool, sign_mask: int,
     stochastic_round_to_element with Philox bits of each element's input
     index; else round to nearest even.  The block exponent is chosen exactly
     as in mx_quantize (from the rotated block's amax).
+
+    first_row, first_col, total_cols: x may be the window of a larger
+    row-major tensor (total_cols columns) whose top-left element is
+    (first_row, first_col); the random bits then follow each element's index
+    in that tensor.
     """
     xf = np.asarray(x, dtype=np.float32)
     R, C = xf.shape
-    idx = (np.arange(R, dtype=np.uint64)[:, None] * np.uint64(C)
-           + np.arange(C, dtype=np.uint64)[None, :])
+    ncol = C if total_cols is None else int(total_cols)
+    idx = ((np.uint64(first_row) + np.arange(R, dtype=np.uint64))[:, None] * np.uint64(ncol)
+           + np.uint64(first_col) + np.arange(C, dtype=np.uint64)[None, :])
     src, sidx = (xf, idx) if axis == "row" else (xf.T, idx.T)
     rows, cols = src.shape
     blocks = src.reshape(rows, cols // BLOCK, BLOCK)

@@ -99,7 +99,8 @@ extern "C" mxq_status mxq_check(void* stream) {
     return MXQ_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return MXQ_ERR_CUDA;
-  const uint32_t words[3] = {take_quant_error(), take_gemm_error(), take_debug_error()};
+  const uint32_t words[4] = {take_quant_error(), take_ablation_error(), take_gemm_error(),
+                             take_debug_error()};
   for (uint32_t w : words)
     if (w) return static_cast<mxq_status>(w & 0xFFu);
   return MXQ_OK;

@@ -22,6 +22,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled();
 
 // Read and clear the device error word of each translation unit.
 uint32_t take_quant_error();
+uint32_t take_ablation_error();
 uint32_t take_gemm_error();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

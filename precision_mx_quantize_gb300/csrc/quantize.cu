@@ -1,423 +1,17 @@
 // MX quantizers (row-wise, column-wise transposed, dual) with the optional
-// fixed 32-point Hadamard rotation, and the dequantizer.
+// fixed 32-point Hadamard rotation, and the dequantizer: the deterministic
+// instantiations of the kernel in quant_kernel.cuh and the C entry points.
 //
 // Operation: "AMD顛覆行業認知！終于攻克FP4大模型訓練致命難題", §02 -- blocks with
 // their own dynamic exponent (microscaling) and a deterministic Hadamard
 // rotation before the MXFP4 quantization of the Wgrad operands;
 // "MindSpeed LLM FSDP2量化特性：低比特大模型训练完全指南", 第 1 步 -- block size
 // 32, E4M3 elements.  Bit-level rules: OCP MX v1.0 / OCP FP8.
-//
-// Design (HBM-bound): a persistent grid of 2 CTAs per SM.  Thread 0 of each
-// CTA streams 128x128 bf16 tiles into a 2-stage shared-memory ring with TMA
-// (128-byte swizzle, two 64-column boxes per tile); all 8 warps read the tile
-// from shared memory:
-//   row path: a thread owns the same 32-column block of rows r and r+64,
-//             so both blocks travel through the packed fp32x2 ALU together;
-//   col path: a thread owns the same 32-row block of two adjacent columns.
-// Each block is (optionally) rotated in registers, its amax reduced, its
-// E8M0 exponent taken from the amax bits, and its elements converted with
-// the hardware's round-to-nearest-even saturating E4M3/E2M1 conversions.
-// Codes go to a swizzled shared-memory staging tile that one TMA store per
-// layout writes out (the transposed column-wise tile included), so global
-// writes are whole-tile bulk copies; scales leave as one 4-byte word per
-// row or column of the tile.
-#include <string.h>
-
-#include "mxq_common.cuh"
-#include "mxq_host.h"
+#include "quant_kernel.cuh"
 
 namespace mxq {
 
-__device__ uint32_t g_err_quant;
-
 namespace {
-
-constexpr int Q_THREADS = 256;
-constexpr int Q_ROWS = 128;             // tile rows
-constexpr int Q_COLS = 128;             // tile cols (two 64-column swizzled halves)
-constexpr int Q_HALF = Q_ROWS * 128;    // bytes of one half: 128 rows of 128 B
-constexpr int Q_TILE = 2 * Q_HALF;      // 32 KB of bf16
-constexpr int Q_STAGES = 2;
-constexpr int Q_STAGE_OUT = 16384;      // staging of one layout's codes (<= 128 x 128 B)
-constexpr int Q_OFF_OUT_R = Q_STAGES * Q_TILE;
-constexpr int Q_OFF_OUT_C = Q_OFF_OUT_R + Q_STAGE_OUT;
-constexpr int Q_OFF_SC_R = Q_OFF_OUT_C + Q_STAGE_OUT;   // 128 rows x 4 scale bytes
-constexpr int Q_OFF_SC_C = Q_OFF_SC_R + 512;            // 128 cols x 4 scale bytes
-constexpr int Q_OFF_BAR = Q_OFF_SC_C + 512;
-constexpr int Q_SMEM = Q_OFF_BAR + 64 + 1024;
-
-struct QArgs {
-  int64_t R, C;
-  int32_t n_ct, n_tiles;
-  uint8_t* scales_r;
-  uint8_t* scales_c;
-  uint64_t timeout_ns;
-};
-
-template <int FMT>
-struct Elem;
-template <>
-struct Elem<MXQ_E4M3> {
-  static constexpr uint32_t emax = 8;  // 448 = 1.75 * 2^8
-  static constexpr int words = 8;      // 32 one-byte codes
-};
-template <>
-struct Elem<MXQ_E5M2> {
-  static constexpr uint32_t emax = 15;  // 57344 = 1.75 * 2^15
-  static constexpr int words = 8;       // 32 one-byte codes
-};
-template <>
-struct Elem<MXQ_E2M1> {
-  static constexpr uint32_t emax = 2;  // 6 = 1.5 * 2^2
-  static constexpr int words = 4;      // 32 four-bit codes
-};
-
-// RN_fp32(2^-2.5) = RN_fp32(sqrt(2)) / 8: the normalization of H_32.
-MXQ_DEV float hadamard_c() { return __uint_as_float(0x3E3504F3u); }
-
-// E8M0 byte from the magnitude bits of the block amax (fp32 layout):
-// floor(log2 amax) - emax + 127 = biased_exponent - emax, clamped at 0
-// (zero and subnormal maxima included); 255 for NaN / Inf.
-MXQ_DEV uint32_t scale_of(uint32_t abits, uint32_t emax) {
-  if (abits >= 0x7F800000u) return 255u;
-  const uint32_t E = abits >> 23;
-  return E > emax ? E - emax : 0u;
-}
-
-// 2^(127 - s), always a normal fp32 for the scales the quantizer produces
-// (s <= 252); 1 for a NaN block whose codes are discarded.
-MXQ_DEV float inv_scale(uint32_t s) {
-  return s == 255u ? 1.0f : __uint_as_float((254u - s) << 23);
-}
-
-// Packed fp32x2 arithmetic, each lane rounded to nearest (one instruction
-// per pair, no fused multiply-add).
-MXQ_DEV float2 add2(float2 a, float2 b) {
-  float2 r;
-  asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
-      "add.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return r;
-}
-MXQ_DEV float2 sub2(float2 a, float2 b) {
-  float2 r;
-  asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
-      "sub.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return r;
-}
-MXQ_DEV float2 mul2(float2 a, float2 b) {
-  float2 r;
-  asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
-      "mul.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return r;
-}
-
-// Natural-order radix-2 Walsh-Hadamard butterflies on two independent
-// 32-blocks at once (lane .x and lane .y): stages h = 1, 2, 4, 8, 16, every
-// add/subtract rounded to nearest, no fused multiply-add.  The final
-// multiply by c is left to the caller.
-MXQ_DEV void fwht32_pair(float2 (&v)[32]) {
-#pragma unroll
-  for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if ((j & h) == 0) {
-        const float2 a = v[j], b = v[j + h];
-        v[j] = add2(a, b);
-        v[j + h] = sub2(a, b);
-      }
-    }
-  }
-}
-
-// Quantize two 32-blocks held lane-wise in v.  For the unrotated path the
-// caller passes the amax bits (fp32 layout) of each block.
-//
-// Rotated path: the rotated value is y = RN(a * c) with a the butterfly
-// output.  Its block amax is RN(max|a| * c) (rounding is monotone), and
-// RN(a * c) * 2^(127-s) equals RN(a * (c * 2^(127-s))) whenever the result
-// is a normal fp32; below that both are far under half the smallest element
-// step and encode as a zero of the same sign.  So one multiply by the exact
-// constant c * 2^(127-s) replaces two, except when that constant would be
-// subnormal (s > 250, only for blocks whose amax is above 2^125), where the
-// two multiplies are kept.
-template <int FMT, bool HAD>
-MXQ_DEV void quant_pair(float2 (&v)[32], uint32_t abA, uint32_t abB,
-                        uint32_t (&oA)[Elem<FMT>::words], uint32_t (&oB)[Elem<FMT>::words],
-                        uint32_t& sA, uint32_t& sB) {
-  if constexpr (HAD) {
-    fwht32_pair(v);
-    float mA = fabsf(v[0].x), mB = fabsf(v[0].y);
-#pragma unroll
-    for (int j = 1; j < 31; j += 2) {
-      mA = max3_abs_nan(mA, v[j].x, v[j + 1].x);
-      mB = max3_abs_nan(mB, v[j].y, v[j + 1].y);
-    }
-    mA = max3_abs_nan(mA, v[31].x, v[31].x);
-    mB = max3_abs_nan(mB, v[31].y, v[31].y);
-    const float c = hadamard_c();
-    abA = __float_as_uint(__fmul_rn(mA, c)) & 0x7FFFFFFFu;
-    abB = __float_as_uint(__fmul_rn(mB, c)) & 0x7FFFFFFFu;
-    sA = scale_of(abA, Elem<FMT>::emax);
-    sB = scale_of(abB, Elem<FMT>::emax);
-    const uint32_t sa = sA == 255u ? 0u : sA, sb = sB == 255u ? 0u : sB;
-    if (max(sa, sb) > 250u) {
-      const float2 c2 = make_float2(c, c);
-      const float2 m2 = make_float2(inv_scale(sA), inv_scale(sB));
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = mul2(mul2(v[j], c2), m2);
-    } else {
-      const float2 m2 = make_float2(__fmul_rn(c, inv_scale(sA)), __fmul_rn(c, inv_scale(sB)));
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], m2);
-    }
-  } else {
-    sA = scale_of(abA, Elem<FMT>::emax);
-    sB = scale_of(abB, Elem<FMT>::emax);
-    const float2 m2 = make_float2(inv_scale(sA), inv_scale(sB));
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], m2);  // exact power-of-two scaling
-  }
-  if constexpr (FMT == MXQ_E4M3) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      oA[k] = cvt_e4m3x4(v[4 * k].x, v[4 * k + 1].x, v[4 * k + 2].x, v[4 * k + 3].x);
-      oB[k] = cvt_e4m3x4(v[4 * k].y, v[4 * k + 1].y, v[4 * k + 2].y, v[4 * k + 3].y);
-    }
-  } else if constexpr (FMT == MXQ_E5M2) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      oA[k] = cvt_e5m2x4(v[4 * k].x, v[4 * k + 1].x, v[4 * k + 2].x, v[4 * k + 3].x);
-      oB[k] = cvt_e5m2x4(v[4 * k].y, v[4 * k + 1].y, v[4 * k + 2].y, v[4 * k + 3].y);
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      oA[k] = cvt_e2m1x8(v[8 * k].x, v[8 * k + 1].x, v[8 * k + 2].x, v[8 * k + 3].x,
-                         v[8 * k + 4].x, v[8 * k + 5].x, v[8 * k + 6].x, v[8 * k + 7].x);
-      oB[k] = cvt_e2m1x8(v[8 * k].y, v[8 * k + 1].y, v[8 * k + 2].y, v[8 * k + 3].y,
-                         v[8 * k + 4].y, v[8 * k + 5].y, v[8 * k + 6].y, v[8 * k + 7].y);
-    }
-  }
-  if (sA == 255u) {
-#pragma unroll
-    for (int k = 0; k < Elem<FMT>::words; ++k) oA[k] = 0u;
-  }
-  if (sB == 255u) {
-#pragma unroll
-    for (int k = 0; k < Elem<FMT>::words; ++k) oB[k] = 0u;
-  }
-}
-
-// Byte offset of (row r, byte b of its 128-byte row) in a 128B-swizzled tile.
-MXQ_DEV int swz128(int r, int b) { return r * 128 + ((((b >> 4) ^ (r & 7)) << 4) | (b & 15)); }
-// Byte offset of (row r, byte b of its 64-byte row) in a 64B-swizzled tile.
-MXQ_DEV int swz64(int r, int b) { return r * 64 + (((((b >> 4) ^ (r >> 1)) & 3) << 4) | (b & 15)); }
-
-// Write one block's codes into a staging tile whose rows are 128 B (one-byte
-// codes, 128B swizzle) or 64 B (E2M1, 64B swizzle).
-template <int FMT>
-MXQ_DEV void stage_block(uint8_t* tile, int row, int block, const uint32_t (&o)[Elem<FMT>::words]) {
-  if constexpr (FMT != MXQ_E2M1) {
-    *reinterpret_cast<uint4*>(tile + swz128(row, 32 * block)) = make_uint4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint4*>(tile + swz128(row, 32 * block + 16)) = make_uint4(o[4], o[5], o[6], o[7]);
-  } else {
-    *reinterpret_cast<uint4*>(tile + swz64(row, 16 * block)) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
-
-template <int FMT, bool HAD>
-MXQ_DEV void row_path(const uint8_t* st, uint8_t* out_tile, uint8_t* sc_tile, int64_t C0,
-                      const QArgs& a, int tid) {
-  const int r = tid & 63, q = tid >> 6;
-  if (C0 + 32 * q >= a.C) return;
-  const uint8_t* half = st + (q >> 1) * Q_HALF;
-  const int cb = (q & 1) * 4;
-  uint32_t wa[16], wb[16];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int off = ((cb + i) ^ (r & 7)) << 4;
-    const uint4 A = *reinterpret_cast<const uint4*>(half + r * 128 + off);
-    const uint4 B = *reinterpret_cast<const uint4*>(half + (r + 64) * 128 + off);
-    wa[4 * i] = A.x; wa[4 * i + 1] = A.y; wa[4 * i + 2] = A.z; wa[4 * i + 3] = A.w;
-    wb[4 * i] = B.x; wb[4 * i + 1] = B.y; wb[4 * i + 2] = B.z; wb[4 * i + 3] = B.w;
-  }
-  uint32_t abA = 0, abB = 0;
-  if constexpr (!HAD) {
-    uint32_t ma = wa[0], mb = wb[0];
-#pragma unroll
-    for (int k = 1; k < 16; ++k) {
-      ma = max_abs_bf16x2(ma, wa[k]);
-      mb = max_abs_bf16x2(mb, wb[k]);
-    }
-    abA = max(ma & 0x7FFFu, (ma >> 16) & 0x7FFFu) << 16;
-    abB = max(mb & 0x7FFFu, (mb >> 16) & 0x7FFFu) << 16;
-  }
-  float2 v[32];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    v[2 * k] = make_float2(bf16lo(wa[k]), bf16lo(wb[k]));
-    v[2 * k + 1] = make_float2(bf16hi(wa[k]), bf16hi(wb[k]));
-  }
-  uint32_t oA[Elem<FMT>::words], oB[Elem<FMT>::words], sA, sB;
-  quant_pair<FMT, HAD>(v, abA, abB, oA, oB, sA, sB);
-  stage_block<FMT>(out_tile, r, q, oA);
-  stage_block<FMT>(out_tile, r + 64, q, oB);
-  sc_tile[r * 4 + q] = static_cast<uint8_t>(sA);
-  sc_tile[(r + 64) * 4 + q] = static_cast<uint8_t>(sB);
-}
-
-template <int FMT, bool HAD>
-MXQ_DEV void col_path(const uint8_t* st, uint8_t* out_tile, uint8_t* sc_tile, int64_t R0,
-                      int64_t C0, const QArgs& a, int tid) {
-  const int cp = tid & 63, b = tid >> 6;
-  if (R0 + 32 * b >= a.R || C0 + 2 * cp >= a.C) return;
-  const uint8_t* half = st + (cp >> 5) * Q_HALF;
-  const int pb = (cp & 31) * 4;  // byte of the column pair inside its 128-byte row
-  uint32_t w[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) w[j] = *reinterpret_cast<const uint32_t*>(half + swz128(32 * b + j, pb));
-  uint32_t abA = 0, abB = 0;
-  if constexpr (!HAD) {
-    uint32_t m = w[0];
-#pragma unroll
-    for (int j = 1; j < 32; ++j) m = max_abs_bf16x2(m, w[j]);
-    abA = (m & 0x7FFFu) << 16;
-    abB = ((m >> 16) & 0x7FFFu) << 16;
-  }
-  float2 v[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = make_float2(bf16lo(w[j]), bf16hi(w[j]));
-  uint32_t oA[Elem<FMT>::words], oB[Elem<FMT>::words], sA, sB;
-  quant_pair<FMT, HAD>(v, abA, abB, oA, oB, sA, sB);
-  stage_block<FMT>(out_tile, 2 * cp, b, oA);
-  stage_block<FMT>(out_tile, 2 * cp + 1, b, oB);
-  sc_tile[(2 * cp) * 4 + b] = static_cast<uint8_t>(sA);
-  sc_tile[(2 * cp + 1) * 4 + b] = static_cast<uint8_t>(sB);
-}
-
-// Scale bytes of one tile: 4 per tile row (row-wise) or tile column
-// (column-wise), written as one word when the destination is aligned.
-MXQ_DEV void store_scales(const uint8_t* sc_tile, uint8_t* dst, int64_t n_lines, int64_t line0,
-                          int64_t nsb, int64_t blk0, int64_t nblk_valid, int i) {
-  const int64_t line = line0 + i;
-  if (line >= n_lines) return;
-  uint8_t* d = dst + line * nsb + blk0;
-  const uint32_t w = *reinterpret_cast<const uint32_t*>(sc_tile + 4 * i);
-  if (nblk_valid >= 4 && (reinterpret_cast<uintptr_t>(d) & 3u) == 0) {
-    *reinterpret_cast<uint32_t*>(d) = w;
-  } else {
-    for (int k = 0; k < 4 && k < nblk_valid; ++k) d[k] = static_cast<uint8_t>(w >> (8 * k));
-  }
-}
-
-MXQ_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(x), "r"(y)
-               : "memory");
-}
-MXQ_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-MXQ_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-MXQ_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-MXQ_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-template <bool ROW, bool COL, int FR, bool HR, int FC, bool HC>
-__global__ void __launch_bounds__(Q_THREADS, 2)
-    mx_quant_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tm_r,
-                    const __grid_constant__ CUtensorMap tm_c, const QArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Q_OFF_BAR);
-  uint8_t* out_r = smem + Q_OFF_OUT_R;
-  uint8_t* out_c = smem + Q_OFF_OUT_C;
-  uint8_t* sc_r = smem + Q_OFF_SC_R;
-  uint8_t* sc_c = smem + Q_OFF_SC_C;
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    prefetch_tmap(&tmap);
-    if constexpr (ROW) prefetch_tmap(&tm_r);
-    if constexpr (COL) prefetch_tmap(&tm_c);
-#pragma unroll
-    for (int s = 0; s < Q_STAGES; ++s) mbar_init(smem_u32(&bars[s]), 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  auto issue = [&](int t, int s) {
-    const int rt = t / a.n_ct, ct = t - rt * a.n_ct;
-    const uint32_t bar = smem_u32(&bars[s]);
-    const uint32_t dst = smem_u32(smem + s * Q_TILE);
-    mbar_arrive_expect_tx(bar, Q_TILE);
-    tma_load_2d(dst, &tmap, bar, ct * Q_COLS, rt * Q_ROWS);
-    tma_load_2d(dst + Q_HALF, &tmap, bar, ct * Q_COLS + 64, rt * Q_ROWS);
-  };
-  if (tid == 0) {
-    for (int s = 0; s < Q_STAGES; ++s) {
-      const int t = blockIdx.x + s * gridDim.x;
-      if (t < a.n_tiles) issue(t, s);
-    }
-  }
-
-  const int64_t nsb_r = a.C >> 5, nsb_c = a.R >> 5;
-  int it = 0;
-  bool failed = false;
-  for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
-    const int s = it % Q_STAGES;
-    const uint32_t parity = (it / Q_STAGES) & 1;
-    const bool ok = mbar_wait(smem_u32(&bars[s]), parity, a.timeout_ns);
-    if (tid == 0) bulk_wait_read0();  // the previous tile's stores have read the staging
-    if (!__syncthreads_and(ok)) {
-      failed = true;
-      break;
-    }
-    const int rt = t / a.n_ct, ct = t - rt * a.n_ct;
-    const int64_t R0 = int64_t(rt) * Q_ROWS, C0 = int64_t(ct) * Q_COLS;
-    const uint8_t* st = smem + s * Q_TILE;
-    if constexpr (ROW) row_path<FR, HR>(st, out_r, sc_r, C0, a, tid);
-    if constexpr (COL) col_path<FC, HC>(st, out_c, sc_c, R0, C0, a, tid);
-    fence_async_smem();
-    __syncthreads();  // staging complete; stage s fully read
-    if (tid == 0) {
-      if constexpr (ROW)
-        tma_store_2d(&tm_r, smem_u32(out_r), static_cast<int32_t>(FR != MXQ_E2M1 ? C0 : C0 / 2),
-                     static_cast<int32_t>(R0));
-      if constexpr (COL)
-        tma_store_2d(&tm_c, smem_u32(out_c), static_cast<int32_t>(FC != MXQ_E2M1 ? R0 : R0 / 2),
-                     static_cast<int32_t>(C0));
-      bulk_commit();
-      const int tn = t + Q_STAGES * gridDim.x;
-      if (tn < a.n_tiles) issue(tn, s);
-    }
-    if constexpr (ROW) {
-      if (tid < Q_ROWS)
-        store_scales(sc_r, a.scales_r, a.R, R0, nsb_r, C0 >> 5, (a.C - C0 + 31) >> 5, tid);
-    }
-    if constexpr (COL) {
-      if (tid >= Q_THREADS - Q_COLS)
-        store_scales(sc_c, a.scales_c, a.C, C0, nsb_c, R0 >> 5, (a.R - R0 + 31) >> 5,
-                     tid - (Q_THREADS - Q_COLS));
-    }
-  }
-  if (tid == 0) bulk_wait0();
-  if (failed && tid == 0) {
-    record_error(&g_err_quant, MXQ_ERR_TIMEOUT, SITE_QUANT_FULL);
-    // Give copies still in flight into this CTA's shared memory a bounded
-    // chance to land before the CTA exits.
-    for (int k = it; k < it + Q_STAGES; ++k) {
-      const int t = blockIdx.x + k * gridDim.x;
-      if (t >= a.n_tiles) break;
-      if (!mbar_wait(smem_u32(&bars[k % Q_STAGES]), (k / Q_STAGES) & 1, a.timeout_ns))
-        record_error(&g_err_quant, MXQ_ERR_TIMEOUT, SITE_QUANT_DRAIN);
-    }
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Dequantization
@@ -559,11 +153,9 @@ __global__ void __launch_bounds__(128) mx_dequant_cols(const uint8_t* __restrict
 // Host side
 // ---------------------------------------------------------------------------
 
-using QuantKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const QArgs);
-
 template <bool ROW, bool COL, int FR, bool HR, int FC, bool HC>
 QuantKernel kernel_ptr() {
-  return mx_quant_kernel<ROW, COL, FR, HR, FC, HC>;
+  return mx_quant_kernel<ROW, COL, FR, HR, FC, HC, 0>;
 }
 
 // Index: row, col, fr, hr, fc, hc (each 0/1) -> kernel.
@@ -590,90 +182,21 @@ QuantKernel pick(bool row, bool col, int fr, int hr, int fc, int hc) {
 #undef MXQ_K
 }
 
-bool valid_fmt(int f) { return f == MXQ_E4M3 || f == MXQ_E2M1 || f == MXQ_E5M2; }
-
 mxq_status quant_launch(const void* x, int64_t R, int64_t C, bool row, bool col, int fr, int hr,
                         void* codes_r, uint8_t* scales_r, int fc, int hc, void* codes_c,
                         uint8_t* scales_c, void* stream) {
-  if (R < 0 || C < 0) return MXQ_ERR_ARG;
-  if (R == 0 || C == 0) return MXQ_OK;
-  if (R >= (int64_t(1) << 31) || C >= (int64_t(1) << 31)) return MXQ_ERR_ARG;
-  if (!x) return MXQ_ERR_ARG;
-  if (row && (!valid_fmt(fr) || !codes_r || !scales_r)) return MXQ_ERR_ARG;
-  if (col && (!valid_fmt(fc) || !codes_c || !scales_c)) return MXQ_ERR_ARG;
-  if (row && C % 32 != 0) return MXQ_ERR_ARG;
-  if (col && (R % 32 != 0 || C % 8 != 0)) return MXQ_ERR_ARG;
-  if (!aligned16(x) || (row && !aligned16(codes_r)) || (col && !aligned16(codes_c)))
-    return MXQ_ERR_ALIGN;
-
-  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
-  if (!encode) return MXQ_ERR_CUDA;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(C) * 2};
-  const cuuint32_t box[2] = {64, Q_ROWS};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims,
-                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return MXQ_ERR_CUDA;
-
-  // Code outputs: 2-D byte tensors written by TMA stores of 128-row tiles.
-  // Rows of 128 B (E4M3) use the 128-byte swizzle, rows of 64 B (E2M1) the
-  // 64-byte swizzle, matching the staging layout in the kernel.
-  auto code_map = [&](CUtensorMap* m, void* base, int64_t lines, int64_t line_elems,
-                      int fmt) -> CUresult {
-    const int64_t lb = fmt != MXQ_E2M1 ? line_elems : line_elems / 2;
-    const cuuint64_t d[2] = {static_cast<cuuint64_t>(lb), static_cast<cuuint64_t>(lines)};
-    const cuuint64_t st[1] = {static_cast<cuuint64_t>(lb)};
-    const cuuint32_t bx[2] = {fmt != MXQ_E2M1 ? 128u : 64u, static_cast<cuuint32_t>(Q_ROWS)};
-    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, d, st, bx, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  fmt != MXQ_E2M1 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  };
-  CUtensorMap map_r, map_c;
-  memset(&map_r, 0, sizeof(map_r));
-  memset(&map_c, 0, sizeof(map_c));
-  if (row && code_map(&map_r, codes_r, R, C, fr) != CUDA_SUCCESS) return MXQ_ERR_CUDA;
-  if (col && code_map(&map_c, codes_c, C, R, fc) != CUDA_SUCCESS) return MXQ_ERR_CUDA;
-
-  QArgs a;
-  a.R = R;
-  a.C = C;
-  a.n_ct = static_cast<int32_t>((C + Q_COLS - 1) / Q_COLS);
-  const int64_t n_rt = (R + Q_ROWS - 1) / Q_ROWS;
-  if (n_rt * a.n_ct >= (int64_t(1) << 31)) return MXQ_ERR_ARG;
-  a.n_tiles = static_cast<int32_t>(n_rt * a.n_ct);
-  a.scales_r = scales_r;
-  a.scales_c = scales_c;
-  a.timeout_ns = wait_timeout_ns();
-
-  QuantKernel k = pick(row, col, fr, hr ? 1 : 0, fc, hc ? 1 : 0);
-  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM) != cudaSuccess)
-    return MXQ_ERR_CUDA;
-  const int grid = static_cast<int>(std::min<int64_t>(a.n_tiles, int64_t(2) * sm_count()));
-  k<<<grid, Q_THREADS, Q_SMEM, static_cast<cudaStream_t>(stream)>>>(map, map_r, map_c, a);
-  return launch_status();
+  return quant_launch_k(pick(row, col, fr, hr ? 1 : 0, fc, hc ? 1 : 0), x, R, C, row, col, fr,
+                        codes_r, scales_r, fc, codes_c, scales_c, 0u, 0u, stream);
 }
 
 }  // namespace
 
-uint32_t take_quant_error() {
-  uint32_t h = 0;
-  if (cudaMemcpyFromSymbol(&h, g_err_quant, sizeof(h)) != cudaSuccess) return MXQ_ERR_CUDA;
-  if (h) {
-    const uint32_t z = 0;
-    cudaMemcpyToSymbol(g_err_quant, &z, sizeof(z));
-  }
-  return h;
-}
+uint32_t take_quant_error() { return take_error_word(); }
 
 }  // namespace mxq
 
 using namespace mxq;
+
 
 extern "C" mxq_status mxq_quantize(const void* x, int64_t rows, int64_t cols, int layout, int fmt,
                                    void* codes, uint8_t* scales, void* stream) {

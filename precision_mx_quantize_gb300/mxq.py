@@ -7,7 +7,7 @@ library has not been built, every call raises -- there is no CPU fallback.
 Low-level functions keep the C names (``mxq_quantize`` ...) and take raw
 pointers; the tensor-level helpers follow the names of the method's
 statement: ``mx_quantize``, ``hadamard_mx_quantize``, ``mx_quantize_dual``,
-``mx_dequantize``, ``mx_gemm``.
+``mx_quantize_ablation``, ``mx_dequantize``, ``mx_gemm``.
 """
 
 from __future__ import annotations
@@ -38,6 +38,7 @@ SIGNATURES = [
     ("mxq_quantize", _I, [_P, _I64, _I64, _I, _I, _P, _P, _P]),
     ("mxq_hadamard_quantize", _I, [_P, _I64, _I64, _I, _I, _P, _P, _P]),
     ("mxq_quantize_dual", _I, [_P, _I64, _I64, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
+    ("mxq_quantize_ablation", _I, [_P, _I64, _I64, _I, _I, _I, ctypes.c_uint32, _I, _U64, _P, _P, _P]),
     ("mxq_dequantize", _I, [_P, _P, _I64, _I64, _I, _I, _P, _I, _P]),
     ("mxq_gemm", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P, _SZ, _P]),
     ("mxq_gemm_workspace_size", _SZ, [_I64, _I64, _I64, _I]),
@@ -103,6 +104,12 @@ def mxq_quantize_dual(x, rows, cols, fmt_r, had_r, codes_r, scales_r, fmt_c, had
                       scales_c, stream):
     return lib().mxq_quantize_dual(x, rows, cols, fmt_r, had_r, codes_r, scales_r, fmt_c, had_c,
                                    codes_c, scales_c, stream)
+
+
+def mxq_quantize_ablation(x, rows, cols, layout, fmt, hadamard, sign_mask, stochastic, seed, codes,
+                          scales, stream):
+    return lib().mxq_quantize_ablation(x, rows, cols, layout, fmt, hadamard, sign_mask, stochastic,
+                                       seed, codes, scales, stream)
 
 
 def mxq_dequantize(codes, scales, rows, cols, layout, fmt, out, out_dtype, stream):
@@ -182,6 +189,20 @@ def mx_quantize_dual(x: torch.Tensor, fmt_r="e4m3", had_r=False, fmt_c="e2m1", h
                           cr.data_ptr(), sr.data_ptr(), FMTS[fmt_c], int(had_c), cc.data_ptr(),
                           sc.data_ptr(), _stream(x.device)), "mxq_quantize_dual")
     return cr, sr, cc, sc
+
+
+def mx_quantize_ablation(x: torch.Tensor, axis="col", fmt="e2m1", hadamard=True, sign_mask=0,
+                         stochastic=False, seed=0, out=None):
+    """MX quantization with a random-sign Hadamard rotation (sign_mask) and/or
+    stochastic rounding (Philox bits keyed by seed); the ablation of the
+    deterministic path."""
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    codes, scales = out if out is not None else _alloc_codes(x, axis, fmt)
+    _ok(mxq_quantize_ablation(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
+                              int(hadamard), int(sign_mask) & 0xFFFFFFFF, int(stochastic),
+                              int(seed) & 0xFFFFFFFFFFFFFFFF, codes.data_ptr(), scales.data_ptr(),
+                              _stream(x.device)), "mxq_quantize_ablation")
+    return codes, scales
 
 
 def mx_dequantize(codes, scales, rows, cols, axis="row", fmt="e4m3", out_dtype=torch.float32,

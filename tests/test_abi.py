@@ -54,3 +54,12 @@ def test_argument_errors_return_before_device_work(lib):
     # E5M2 is a single-layout format: the dual pass rejects it
     assert mxq.mxq_quantize_dual(p, 64, 64, mxq.E5M2, 0, p, p, E2, 1, p, p, None) == 3
     assert mxq.mxq_quantize(p, 64, 64, ROW, 3, p, p, None) == 1
+    # ablation: a sign mask needs the rotation; the usual shape rules apply
+    A = mxq.mxq_quantize_ablation
+    assert A(p, 64, 64, ROW, E2, 0, 0x5, 1, 7, p, p, None) == 1
+    assert A(p, 64, 48, ROW, E4, 1, 0x5, 1, 7, p, p, None) == 1
+    assert A(p, 40, 64, COL, E2, 0, 0, 1, 7, p, p, None) == 1
+    assert A(p, 64, 64, 5, E4, 1, 0, 1, 7, p, p, None) == 1
+    assert A(p, 64, 64, ROW, 9, 1, 0, 1, 7, p, p, None) == 1
+    assert A(ctypes.c_void_p(16 * 1024 + 2), 64, 64, ROW, E4, 0, 0, 1, 7, p, p, None) == 2
+    assert A(p, 0, 64, ROW, E4, 1, 0xFFFFFFFF, 1, 2 ** 64 - 1, p, p, None) == 0

@@ -144,3 +144,19 @@ def test_stochastic_quantization_is_unbiased_on_average():
     c, s = O.mx_quantize(x, "row", O.E2M1)
     bias_rne = np.abs(O.dequantize_f64(c, s, O.E2M1) - x).mean()
     assert bias_sr < 0.5 * bias_rne
+
+
+def test_window_indices_match_the_full_tensor():
+    # a window of a larger tensor draws the same bits as the full tensor
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((96, 128)).astype(np.float32)
+    for axis in ("row", "col"):
+        full = O.mx_quantize_ablation(x, axis, O.E4M3, True, 0x13579BDF, True, 99)
+        if axis == "row":
+            win = O.mx_quantize_ablation(x[32:64], axis, O.E4M3, True, 0x13579BDF, True, 99,
+                                         first_row=32, total_cols=128)
+            assert np.array_equal(win[0], full[0][32:64]) and np.array_equal(win[1], full[1][32:64])
+        else:
+            win = O.mx_quantize_ablation(x[:, 40:41], axis, O.E4M3, True, 0x13579BDF, True, 99,
+                                         first_col=40, total_cols=128)
+            assert np.array_equal(win[0], full[0][40:41]) and np.array_equal(win[1], full[1][40:41])
