@@ -583,6 +583,58 @@ def _case_bytes(what, args):
     return (M + N) * K * (eb + 1 / 32) + M * N * (4 if od == "f32" else 2)
 
 
+ABLATION_VARIANTS = [
+    # name, hadamard, random sign mask, stochastic rounding
+    ("no rotation, RNE", False, False, False),
+    ("fixed Hadamard, RNE (the method)", True, False, False),
+    ("random-sign Hadamard, RNE", True, True, False),
+    ("no rotation, stochastic rounding", False, False, True),
+    ("fixed Hadamard, stochastic rounding", True, False, True),
+]
+
+
+def ablation_error(tokens=16384, n_out=4096, n_in=4096, draws=8):
+    """Error structure of the MXFP4 Wgrad under the ablation variants.
+
+    dW = dY^T X with dY [tokens, n_out] ~ N(0, 1e-3) x per-column
+    LogNormal(0, 2) and X [tokens, n_in] ~ Student-t(3) x per-channel
+    LogNormal(0, 1) (the Wgrad workload's distributions), both quantized
+    column-wise to E2M1 along tokens and multiplied by the MXFP4 GEMM.
+    Reference: the fp32 product of the bf16 inputs (no TF32).  For each
+    variant: the relative Frobenius error of one draw, and of the mean of
+    `draws` draws (new random signs / seeds per draw): a deterministic
+    variant's error does not shrink with averaging, an unbiased one's does.
+    A quality measurement, not a parity check.
+    """
+    import torch
+
+    from precision_mx_quantize_gb300 import mxq, synth
+    torch.backends.cuda.matmul.allow_tf32 = False
+    dy = synth.out_grad(tokens, n_out, seed=1).cuda()
+    x = synth.activation(tokens, n_in, seed=2).cuda()
+    ref = dy.float().t() @ x.float()
+    nref = ref.norm().item()
+    rng = __import__("random").Random(7)
+    out = {}
+    for name, had, rand_sign, sr in ABLATION_VARIANTS:
+        acc = torch.zeros_like(ref)
+        first = None
+        for d in range(draws):
+            mask = rng.getrandbits(32) if rand_sign else 0
+            seed = 1000 + d
+            A, sA = mxq.mx_quantize_ablation(dy, "col", "e2m1", had, mask, sr, seed)
+            B, sB = mxq.mx_quantize_ablation(x, "col", "e2m1", had, mask, sr, seed + 500)
+            dw = mxq.mx_gemm(A, sA, B, sB, "e2m1", n_out, n_in, tokens)
+            acc += dw
+            if first is None:
+                first = (dw - ref).norm().item() / nref
+        mxq.check()
+        out[name] = {"rel_err_one_draw": round(first, 6),
+                     f"rel_err_mean_of_{draws}": round((acc / draws - ref).norm().item() / nref, 6)}
+    return {"case": "ablate-error", "workload": f"Wgrad dY^T X, tokens={tokens}, out={n_out}, in={n_in}, "
+            "E2M1 column-wise along tokens", "variants": out}
+
+
 def run_case(name, timed=False):
     """Run one kernel case three times (for ncu captures of a single kernel).
 
@@ -593,6 +645,9 @@ def run_case(name, timed=False):
     import torch
 
     from precision_mx_quantize_gb300 import mxq
+    if name == "ablate-error":
+        print(json.dumps(ablation_error()))
+        return
     what, args = CASES[name]
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
@@ -657,7 +712,9 @@ def main():
     ap.add_argument("--tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
-    ap.add_argument("--case", choices=sorted(CASES), help="run one kernel case (for ncu) and exit")
+    ap.add_argument("--case", choices=sorted(CASES) + ["ablate-error"],
+                    help="run one kernel case (for ncu) and exit; ablate-error prints the "
+                         "Wgrad error of the rotation / rounding variants")
     ap.add_argument("--timed", action="store_true", help="with --case: time the case's launches")
     args = ap.parse_args()
     if args.case:

@@ -160,3 +160,30 @@ def test_window_indices_match_the_full_tensor():
             win = O.mx_quantize_ablation(x[:, 40:41], axis, O.E4M3, True, 0x13579BDF, True, 99,
                                          first_col=40, total_cols=128)
             assert np.array_equal(win[0], full[0][40:41]) and np.array_equal(win[1], full[1][40:41])
+
+
+def test_error_structure_of_the_variants():
+    # the contrast the AMD FP4 page (§01-§02) rests on, in the oracle at a
+    # small Wgrad shape: on heavy-tailed tokens the fixed rotation lowers the
+    # MXFP4 error of dY^T X; deterministic variants repeat the same error
+    # every draw, stochastic rounding averages it away
+    rng = np.random.default_rng(8)
+    T, n_out, n_in = 512, 48, 40
+    dy = (rng.standard_t(3, (T, n_out)) * 1e-3).astype(np.float32)
+    x = rng.standard_t(3, (T, n_in)).astype(np.float32)
+    ref = dy.astype(np.float64).T @ x.astype(np.float64)
+
+    def err(had, mask, sr, seed):
+        A, sA = O.mx_quantize_ablation(dy, "col", O.E2M1, had, mask, sr, seed)
+        B, sB = O.mx_quantize_ablation(x, "col", O.E2M1, had, mask, sr, seed + 1)
+        c, _ = O.mx_gemm_f64(A, sA, B, sB, O.E2M1)
+        return c
+
+    rel = lambda c: np.linalg.norm(c - ref) / np.linalg.norm(ref)
+    plain = err(False, 0, False, 0)
+    fixed = err(True, 0, False, 0)
+    assert rel(fixed) < rel(plain)
+    assert np.array_equal(err(True, 0, False, 5), fixed)        # deterministic
+    draws = [err(True, 0, True, 100 + 2 * d) for d in range(8)]
+    one, mean8 = rel(draws[0]), rel(np.mean(draws, axis=0))
+    assert mean8 < 0.6 * one                                    # unbiased: averages down
