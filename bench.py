@@ -563,6 +563,11 @@ CASES = {
     "gemm-e2m1": ("gemm", (8192, 8192, 8192, "e2m1", "bf16")),
     "quant-dual-e4m3-he2m1": ("quant", (16384, 8192, "e4m3", False, "e2m1", True)),
     "quant-dual-he2m1-he2m1": ("quant", (16384, 8192, "e2m1", True, "e2m1", True)),
+    # the epilogue writing E4M3 codes of the product, and the unfused pair it
+    # replaces (bf16 product, then a row-wise E4M3 quantizer pass over it)
+    "gemm-e4m3-q": ("gemmq", (8192, 8192, 4096, "e4m3", "e4m3")),
+    "gemm-e4m3-bf16": ("gemm", (8192, 8192, 4096, "e4m3", "bf16")),
+    "quant-row-e4m3": ("quant1", (8192, 8192, "row", "e4m3")),
     # ablation: column-wise random-sign Hadamard E2M1 with stochastic rounding
     "ablate-col-rhe2m1-sr": ("ablate", (16384, 8192, "col", "e2m1", True, 0xA5A5F00F, True)),
     "ablate-row-e4m3-sr": ("ablate", (16384, 8192, "row", "e4m3", False, 0, True)),
@@ -578,9 +583,16 @@ def _case_bytes(what, args):
     if what == "ablate":
         R, C, _, f, _, _, _ = args
         return 2 * R * C + R * C * (0.5 if f == "e2m1" else 1.0) + R * C / 32
+    if what == "quant1":
+        R, C, _, f = args
+        return 2 * R * C + R * C * (0.5 if f == "e2m1" else 1.0) + R * C / 32
     M, N, K, fmt, od = args
-    eb = 1.0 if fmt == "e4m3" else 0.5
-    return (M + N) * K * (eb + 1 / 32) + M * N * (4 if od == "f32" else 2)
+    eb = 1.0 if fmt != "e2m1" else 0.5
+    if what == "gemmq":
+        out = M * N * ((0.5 if od == "e2m1" else 1.0) + 1 / 32)
+    else:
+        out = M * N * (4 if od == "f32" else 2)
+    return (M + N) * K * (eb + 1 / 32) + out
 
 
 ABLATION_VARIANTS = [
@@ -651,7 +663,7 @@ def run_case(name, timed=False):
     what, args = CASES[name]
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
-    if what == "gemm":
+    if what in ("gemm", "gemmq"):
         M, N, K, fmt, od = args
         kb = K if fmt == "e4m3" else K // 2
         hi = 0x7E if fmt == "e4m3" else 256
@@ -659,22 +671,33 @@ def run_case(name, timed=False):
         B = torch.randint(0, hi, (N, kb), dtype=torch.uint8, device="cuda", generator=g)
         sA = torch.randint(120, 134, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
         sB = torch.randint(120, 134, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
-        dt = torch.float32 if od == "f32" else torch.bfloat16
-        C = torch.empty((M, N), dtype=dt, device="cuda")
         ws = mxq.gemm_workspace(M, N, K, fmt, "cuda")
-        launch = lambda: mxq.mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=dt, out=C, workspace=ws)
+        if what == "gemmq":
+            q = mxq.mx_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt=od, workspace=ws)
+            launch = lambda: mxq.mx_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt=od, out=q,
+                                                  workspace=ws)
+        else:
+            dt = torch.float32 if od == "f32" else torch.bfloat16
+            C = torch.empty((M, N), dtype=dt, device="cuda")
+            launch = lambda: mxq.mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=dt, out=C,
+                                         workspace=ws)
     elif what == "quant":
         R, Cc, fr, hr, fc, hc = args
         x = torch.randn(R, Cc, device="cuda", generator=g).to(torch.bfloat16)
         out = mxq.mx_quantize_dual(x, fr, hr, fc, hc)
         launch = lambda: mxq.mx_quantize_dual(x, fr, hr, fc, hc, out=out)
+    elif what == "quant1":
+        R, Cc, axis, f = args
+        x = torch.randn(R, Cc, device="cuda", generator=g).to(torch.bfloat16)
+        out = mxq.mx_quantize(x, axis, f)
+        launch = lambda: mxq.mx_quantize(x, axis, f, out=out)
     else:
         R, Cc, axis, f, had, mask, sr = args
         x = torch.randn(R, Cc, device="cuda", generator=g).to(torch.bfloat16)
         out = mxq.mx_quantize_ablation(x, axis, f, had, mask, sr, 1)
         launch = lambda: mxq.mx_quantize_ablation(x, axis, f, had, mask, sr, 1, out=out)
     if not timed:
-        for _ in range(3 if what == "gemm" else 2):
+        for _ in range(3 if what in ("gemm", "gemmq") else 2):
             launch()
         mxq.check()
         print(json.dumps({"case": name, "status": "ok"}))
@@ -693,7 +716,7 @@ def run_case(name, timed=False):
     ms = e0.elapsed_time(e1) / n
     peaks = _peaks()
     line = {"case": name, "ms_per_launch": round(ms, 4)}
-    if what == "gemm":
+    if what in ("gemm", "gemmq"):
         M, N, K, fmt, _ = args
         tf = 2 * M * N * K / ms / 1e9
         line.update({"TFLOP/s": round(tf, 1)})

@@ -186,6 +186,26 @@ mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, const uint8
                     int64_t M, int64_t N, int64_t K, void* C, int out_dtype,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * mxq_gemm whose epilogue writes the product as row-wise MX codes instead of
+ * fp32/bf16: the next layer's operand straight from the accumulators, with
+ * no bf16 round trip through memory (a GEMM fused with its consumer's
+ * quantization, in the spirit of the fused kernels -- fused MLP among them --
+ * that [LUMEN] §2 "AITER高性能内核集成" lists).
+ * The fp32 accumulators of each output row are split into 32-column blocks;
+ * each block gets the shared exponent of its fp32 amax and its elements are
+ * rounded to out_fmt by the rules of mxq_quantize (the conventions at the
+ * top of this file), without rounding the fp32 values to bf16 first.
+ * A, sA, B, sB, fmt, M, N, K, workspace: as mxq_gemm.
+ * out_fmt: MXQ_E4M3, MXQ_E5M2 or MXQ_E2M1.  N % 32 == 0 (MXQ_ERR_ARG).
+ * out_codes: [M][N] bytes (E2M1: [M][N/2]), 16-byte aligned (MXQ_ERR_ALIGN);
+ * out_scales: [M][N/32], any alignment.  The layout is MXQ_ROWWISE's.
+ */
+mxq_status mxq_gemm_quantize(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                             int fmt, int64_t M, int64_t N, int64_t K, int out_fmt,
+                             void* out_codes, uint8_t* out_scales, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace mxq_gemm needs for this problem (0 on bad arguments). */
 size_t mxq_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int fmt);
 

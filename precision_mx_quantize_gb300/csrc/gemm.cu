@@ -76,6 +76,10 @@ struct GArgs {
   int32_t fp4;
   int32_t elem_code;            // A/B element type field of the instruction descriptor
   int32_t wide_stores;          // rows of C are 32-byte aligned: 256-bit stores
+  int32_t out_q;                // 1: C receives row-wise MX codes of the product
+  int32_t q_fmt;                // their element format
+  uint8_t* q_scales;            // their E8M0 scales [M][N/32]
+  int32_t q_scale_words;        // scale rows are 4-byte aligned: one word per 4 blocks
   uint64_t timeout_ns;
 };
 
@@ -243,6 +247,68 @@ MXQ_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
+}
+
+// Row-wise MX quantization of the 128 fp32 accumulators a thread holds for
+// one output row (four 32-column blocks, nblk of them inside N): per block
+// the amax of the fp32 values, its E8M0 exponent, the exact power-of-two
+// scaling and the round-to-nearest-even saturating conversion -- the rules
+// of the quantizer, applied to the fp32 product without a bf16 rounding.
+template <int QF>
+MXQ_DEV void store_row_codes(const uint32_t (&v)[128], const GArgs& a, int64_t row, int64_t col0,
+                             int nblk) {
+  constexpr uint32_t emax = QF == MXQ_E4M3 ? 8u : (QF == MXQ_E5M2 ? 15u : 2u);
+  constexpr int cb = QF == MXQ_E2M1 ? 16 : 32;   // code bytes per block
+  const int64_t row_bytes = QF == MXQ_E2M1 ? int64_t(a.N) / 2 : int64_t(a.N);
+  uint8_t* crow = static_cast<uint8_t*>(a.C) + row * row_bytes + (col0 / 32) * cb;
+  uint32_t sw = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    if (b < nblk) {
+      const uint32_t* x = v + 32 * b;
+      float m = fabsf(__uint_as_float(x[0]));
+#pragma unroll
+      for (int j = 1; j < 31; j += 2)
+        m = max3_abs_nan(m, __uint_as_float(x[j]), __uint_as_float(x[j + 1]));
+      m = max3_abs_nan(m, __uint_as_float(x[31]), __uint_as_float(x[31]));
+      const uint32_t sc = scale_of(__float_as_uint(m) & 0x7FFFFFFFu, emax);
+      const float k = inv_scale(sc);
+      auto f = [&](int j) { return __fmul_rn(__uint_as_float(x[j]), k); };
+      uint32_t w[8];
+      if constexpr (QF == MXQ_E2M1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          w[q] = cvt_e2m1x8(f(8 * q), f(8 * q + 1), f(8 * q + 2), f(8 * q + 3), f(8 * q + 4),
+                            f(8 * q + 5), f(8 * q + 6), f(8 * q + 7));
+      } else if constexpr (QF == MXQ_E5M2) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[q] = cvt_e5m2x4(f(4 * q), f(4 * q + 1), f(4 * q + 2), f(4 * q + 3));
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[q] = cvt_e4m3x4(f(4 * q), f(4 * q + 1), f(4 * q + 2), f(4 * q + 3));
+      }
+      if (sc == 255u) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[q] = 0u;
+      }
+      uint8_t* dst = crow + b * cb;
+      if constexpr (QF == MXQ_E2M1) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else if (a.wide_stores) {
+        st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+      } else {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      sw |= sc << (8 * b);
+    }
+  }
+  uint8_t* srow = a.q_scales + row * (int64_t(a.N) / 32) + col0 / 32;
+  if (a.q_scale_words && nblk == 4) {
+    *reinterpret_cast<uint32_t*>(srow) = sw;
+  } else {
+    for (int b = 0; b < nblk; ++b) srow[b] = static_cast<uint8_t>(sw >> (8 * b));
+  }
 }
 
 // Work item t -> (mp, nt).  Tiles are visited in groups of `group` rows (or
@@ -489,7 +555,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const int64_t col0 = int64_t(nt) * G_BN + colh * 128;
       if (row < a.M && col0 < a.N) {
         const int64_t ncols = (a.N - col0) < 128 ? (a.N - col0) : 128;
-        if (a.out_bf16) {
+        if (a.out_q) {
+          const int nblk = static_cast<int>(ncols >> 5);   // N % 32 == 0
+          if (a.q_fmt == MXQ_E2M1) store_row_codes<MXQ_E2M1>(v, a, row, col0, nblk);
+          else if (a.q_fmt == MXQ_E5M2) store_row_codes<MXQ_E5M2>(v, a, row, col0, nblk);
+          else store_row_codes<MXQ_E4M3>(v, a, row, col0, nblk);
+        } else if (a.out_bf16) {
           __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(a.C) + row * a.N + col0;
           uint32_t p[64];
 #pragma unroll
@@ -630,16 +701,26 @@ extern "C" size_t mxq_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int f
   return static_cast<size_t>(p.ws_a + p.ws_b);
 }
 
-extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
-                               int fmt, int64_t M, int64_t N, int64_t K, void* C, int out_dtype,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+// What the epilogue writes: C as fp32 or bf16, or row-wise MX codes of C
+// (q_fmt) with their scales.
+struct OutSpec {
+  void* C;
+  int kind;            // 0: fp32, 1: bf16, 2: MX codes
+  int q_fmt;
+  uint8_t* q_scales;
+};
+
+mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, int fmt,
+                       int64_t M, int64_t N, int64_t K, const OutSpec& out, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  void* C = out.C;
   Plan p;
   if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
   if (!A || !sA || !B || !sB || !C || !workspace) return MXQ_ERR_ARG;
-  if (out_dtype != MXQ_OUT_F32 && out_dtype != MXQ_OUT_BF16) return MXQ_ERR_ARG;
   if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
     return MXQ_ERR_ARG;
-  if (N % (out_dtype == MXQ_OUT_F32 ? 4 : 8) != 0) return MXQ_ERR_ALIGN;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return MXQ_ERR_ALIGN;
@@ -734,16 +815,22 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   a.sfa = ws;
   a.sfb = ws + p.ws_a;
   a.C = C;
-  a.out_bf16 = out_dtype == MXQ_OUT_BF16;
+  a.out_bf16 = out.kind == 1;
+  a.out_q = out.kind == 2;
+  a.q_fmt = out.q_fmt;
+  a.q_scales = out.q_scales;
+  a.q_scale_words = (reinterpret_cast<uintptr_t>(out.q_scales) & 3u) == 0 && (N / 32) % 4 == 0;
   a.fp4 = fmt == MXQ_E2M1;
   // kind::mxf8f6f4 element types: E4M3 = 0, E5M2 = 1; kind::mxf4: E2M1 = 1
   a.elem_code = fmt == MXQ_E4M3 ? 0 : 1;
-  a.wide_stores = (reinterpret_cast<uintptr_t>(C) & 31u) == 0 &&
-                  N % (out_dtype == MXQ_OUT_F32 ? 8 : 16) == 0;
+  // 256-bit stores need 32-byte aligned rows: fp32 rows of N % 8 == 0,
+  // bf16 rows of N % 16 == 0, one-byte code rows of N % 32 == 0
+  const int wide_mult = out.kind == 0 ? 8 : (out.kind == 1 ? 16 : 32);
+  a.wide_stores = (reinterpret_cast<uintptr_t>(C) & 31u) == 0 && N % wide_mult == 0;
   a.timeout_ns = wait_timeout_ns();
   // every field the kernel dereferences or divides by is set
   if (!a.C || !a.sfa || !a.sfb || a.nk <= 0 || a.kc_per_row <= 0 || a.group <= 0 ||
-      a.n_tiles <= 0 || a.n_nt <= 0 || a.n_mp <= 0)
+      a.n_tiles <= 0 || a.n_nt <= 0 || a.n_mp <= 0 || (a.out_q && !a.q_scales))
     return MXQ_ERR_ARG;
 
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(mx_gemm_kernel),
@@ -765,6 +852,33 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   cfg.gridDim = dim3(static_cast<unsigned>(G_CLUSTER * std::min(a.n_tiles, max_clusters)), 1, 1);
   if (cudaLaunchKernelEx(&cfg, mx_gemm_kernel, ta, tb, tsa, tsb, a) != cudaSuccess) return MXQ_ERR_CUDA;
   return launch_status();
+}
+
+}  // namespace
+
+extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                               int fmt, int64_t M, int64_t N, int64_t K, void* C, int out_dtype,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (out_dtype != MXQ_OUT_F32 && out_dtype != MXQ_OUT_BF16) return MXQ_ERR_ARG;
+  Plan p;
+  if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
+  if (N % (out_dtype == MXQ_OUT_F32 ? 4 : 8) != 0) return MXQ_ERR_ALIGN;
+  const OutSpec out{C, out_dtype == MXQ_OUT_BF16 ? 1 : 0, 0, nullptr};
+  return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream);
+}
+
+extern "C" mxq_status mxq_gemm_quantize(const void* A, const uint8_t* sA, const void* B,
+                                        const uint8_t* sB, int fmt, int64_t M, int64_t N,
+                                        int64_t K, int out_fmt, void* out_codes,
+                                        uint8_t* out_scales, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (out_fmt != MXQ_E4M3 && out_fmt != MXQ_E5M2 && out_fmt != MXQ_E2M1) return MXQ_ERR_ARG;
+  if (!out_scales) return MXQ_ERR_ARG;
+  Plan p;
+  if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
+  if (N % 32 != 0) return MXQ_ERR_ARG;
+  const OutSpec out{out_codes, 2, out_fmt, out_scales};
+  return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -112,6 +112,22 @@ MXQ_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---- shared exponents -------------------------------------------------------
+// E8M0 byte from the magnitude bits of the block amax (fp32 layout):
+// floor(log2 amax) - emax + 127 = biased_exponent - emax, clamped at 0
+// (zero and subnormal maxima included); 255 for NaN / Inf.
+MXQ_DEV uint32_t scale_of(uint32_t abits, uint32_t emax) {
+  if (abits >= 0x7F800000u) return 255u;
+  const uint32_t E = abits >> 23;
+  return E > emax ? E - emax : 0u;
+}
+
+// 2^(127 - s), always a normal fp32 for the scales the quantizer produces
+// (s <= 252); 1 for a NaN block whose codes are discarded.
+MXQ_DEV float inv_scale(uint32_t s) {
+  return s == 255u ? 1.0f : __uint_as_float((254u - s) << 23);
+}
+
 // ---- element conversions ----------------------------------------------------
 // Four fp32 values -> four E4M3 codes (round to nearest even, saturating),
 // a0 in the lowest byte.

@@ -97,21 +97,6 @@ struct Elem<MXQ_E2M1> {
 // RN_fp32(2^-2.5) = RN_fp32(sqrt(2)) / 8: the normalization of H_32.
 MXQ_DEV float hadamard_c() { return __uint_as_float(0x3E3504F3u); }
 
-// E8M0 byte from the magnitude bits of the block amax (fp32 layout):
-// floor(log2 amax) - emax + 127 = biased_exponent - emax, clamped at 0
-// (zero and subnormal maxima included); 255 for NaN / Inf.
-MXQ_DEV uint32_t scale_of(uint32_t abits, uint32_t emax) {
-  if (abits >= 0x7F800000u) return 255u;
-  const uint32_t E = abits >> 23;
-  return E > emax ? E - emax : 0u;
-}
-
-// 2^(127 - s), always a normal fp32 for the scales the quantizer produces
-// (s <= 252); 1 for a NaN block whose codes are discarded.
-MXQ_DEV float inv_scale(uint32_t s) {
-  return s == 255u ? 1.0f : __uint_as_float((254u - s) << 23);
-}
-
 // Packed fp32x2 arithmetic, each lane rounded to nearest (one instruction
 // per pair, no fused multiply-add).
 MXQ_DEV float2 add2(float2 a, float2 b) {

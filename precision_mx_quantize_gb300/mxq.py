@@ -7,7 +7,7 @@ library has not been built, every call raises -- there is no CPU fallback.
 Low-level functions keep the C names (``mxq_quantize`` ...) and take raw
 pointers; the tensor-level helpers follow the names of the method's
 statement: ``mx_quantize``, ``hadamard_mx_quantize``, ``mx_quantize_dual``,
-``mx_quantize_ablation``, ``mx_dequantize``, ``mx_gemm``.
+``mx_quantize_ablation``, ``mx_dequantize``, ``mx_gemm``, ``mx_gemm_quantize``.
 """
 
 from __future__ import annotations
@@ -41,6 +41,7 @@ SIGNATURES = [
     ("mxq_quantize_ablation", _I, [_P, _I64, _I64, _I, _I, _I, ctypes.c_uint32, _I, _U64, _P, _P, _P]),
     ("mxq_dequantize", _I, [_P, _P, _I64, _I64, _I, _I, _P, _I, _P]),
     ("mxq_gemm", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P, _SZ, _P]),
+    ("mxq_gemm_quantize", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
     ("mxq_gemm_workspace_size", _SZ, [_I64, _I64, _I64, _I]),
     ("mxq_gemm_noalloc", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P]),
     ("mxq_check", _I, [_P]),
@@ -118,6 +119,12 @@ def mxq_dequantize(codes, scales, rows, cols, layout, fmt, out, out_dtype, strea
 
 def mxq_gemm(A, sA, B, sB, fmt, M, N, K, C, out_dtype, workspace, ws_bytes, stream):
     return lib().mxq_gemm(A, sA, B, sB, fmt, M, N, K, C, out_dtype, workspace, ws_bytes, stream)
+
+
+def mxq_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt, codes, scales, workspace, ws_bytes,
+                      stream):
+    return lib().mxq_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt, codes, scales, workspace,
+                                   ws_bytes, stream)
 
 
 def mxq_gemm_noalloc(A, sA, B, sB, fmt, M, N, K, C, out_dtype, stream):
@@ -232,3 +239,20 @@ def mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=torch.float32, out=None, works
                  out.data_ptr(), od, workspace.data_ptr(), workspace.numel(),
                  _stream(A.device)), "mxq_gemm")
     return out
+
+
+def mx_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt="e4m3", out=None, workspace=None):
+    """dec(A) @ dec(B)^T with the epilogue writing row-wise MX codes of the
+    fp32 product (blocks of 32 along N); returns (codes, scales)."""
+    if out is None:
+        cs, ss = code_shape(M, N, "row", out_fmt)
+        out = (torch.empty(cs, dtype=torch.uint8, device=A.device),
+               torch.empty(ss, dtype=torch.uint8, device=A.device))
+    codes, scales = out
+    if workspace is None:
+        workspace = gemm_workspace(M, N, K, fmt, A.device)
+    _ok(mxq_gemm_quantize(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M, N,
+                          K, FMTS[out_fmt], codes.data_ptr(), scales.data_ptr(),
+                          workspace.data_ptr(), workspace.numel(), _stream(A.device)),
+        "mxq_gemm_quantize")
+    return codes, scales

@@ -9,8 +9,19 @@ from precision_mx_quantize_gb300 import build as _build
 from precision_mx_quantize_gb300 import mxq
 
 
-def ensure_built():
+def _stale() -> bool:
     if not os.path.exists(mxq.LIB_PATH):
+        return True
+    built = os.path.getmtime(mxq.LIB_PATH)
+    srcs = _build.sources() + [os.path.join(_build.CSRC, f) for f in os.listdir(_build.CSRC)
+                               if f.endswith((".cuh", ".h"))]
+    srcs += [os.path.join(_build.INCLUDE, f) for f in os.listdir(_build.INCLUDE)]
+    return any(os.path.getmtime(f) > built for f in srcs)
+
+
+def ensure_built():
+    """Build the library if it is missing or older than any of its sources."""
+    if _stale():
         _build.build()
     return mxq.lib()
 
