@@ -490,8 +490,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       // Copy each stage's scales into both CTAs' tensor memory ahead of the
       // MMA lane and signal it through sf_ready (two arrivals per stage).
       // Separate threads, because every tcgen05 instruction occupies its
-      // issuing thread for ~100 cycles: warp 10 copies the A scales and the
-      // scales of B rows 0-127, warp 11 those of B rows 128-255.
+      // issuing thread for ~70-100 cycles.  E4M3: warp 10 copies the A
+      // scales and those of B rows 0-127, warp 11 those of B rows 128-255.
+      // E2M1 (twice the chunks): warp 10 the two A chunks and the first B
+      // chunk, warp 11 the other three.
       const bool first = warp == 10;
       const uint32_t st0 = smem_u32(smem);
       const bool fp4 = a.fp4 != 0;
@@ -510,17 +512,23 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const uint32_t sfa_t = tmem + G_SFA_COL0 + 8 * s;
         const uint32_t sfb_t = tmem + G_SFB_COL0 + 16 * s;
         // A: chunk c -> columns +4c.  B: k-chunk c of rows 0-127 -> +8c,
-        // rows 128-255 -> +8c+4 (rows 128-255 start sf_bytes_a into the slot)
-        if (first) {
+        // rows 128-255 -> +8c+4 (rows 128-255 start sf_bytes_a into the slot).
+        // E4M3: 3 chunks per stage (2 + 1); E2M1: 6 chunks (3 + 3).
+        if (fp4) {
+          if (first) {
+            tc_cp_sf_pair(sfa_t, sfa_smem);
+            tc_cp_sf_pair(sfa_t + 4, sfa_smem + 512);
+            tc_cp_sf_pair(sfb_t, sfb_smem);
+          } else {
+            tc_cp_sf_pair(sfb_t + 8, sfb_smem + 512);
+            tc_cp_sf_pair(sfb_t + 4, sfb_smem + sf_bytes_a);
+            tc_cp_sf_pair(sfb_t + 12, sfb_smem + sf_bytes_a + 512);
+          }
+        } else if (first) {
           tc_cp_sf_pair(sfa_t, sfa_smem);
           tc_cp_sf_pair(sfb_t, sfb_smem);
-          if (fp4) {
-            tc_cp_sf_pair(sfa_t + 4, sfa_smem + 512);
-            tc_cp_sf_pair(sfb_t + 8, sfb_smem + 512);
-          }
         } else {
           tc_cp_sf_pair(sfb_t + 4, sfb_smem + sf_bytes_a);
-          if (fp4) tc_cp_sf_pair(sfb_t + 12, sfb_smem + sf_bytes_a + 512);
         }
         tc_commit_pair_mc(smem_u32(&sf_ready[s]), 0x1);
         if (++s == G_STAGES) { s = 0; phase ^= 1; }
