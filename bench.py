@@ -182,9 +182,11 @@ def build_device_state(plan, device):
         st["dy"] = d["dy"].to(device)
 
         def codes(rows, cols, axis, fmt):
-            cs, ss = mxq.code_shape(rows, cols, axis, fmt)
+            cs, _ = mxq.code_shape(rows, cols, axis, fmt)
+            lines, blocked = (rows, cols) if axis == "row" else (cols, rows)
             return (torch.empty(cs, dtype=torch.uint8, device=device),
-                    torch.empty(ss, dtype=torch.uint8, device=device))
+                    torch.empty(mxq.mxq_scales_tc_bytes(lines, blocked), dtype=torch.uint8,
+                                device=device))
 
         st["xq"] = (*codes(T, fin, "row", "e4m3"), *codes(T, fin, "col", "e2m1"))
         st["wq"] = (*codes(fout, fin, "row", "e4m3"), *codes(fout, fin, "col", "e4m3"))
@@ -192,16 +194,15 @@ def build_device_state(plan, device):
         st["y"] = torch.empty((T, fout), dtype=torch.bfloat16, device=device)
         st["dx"] = torch.empty((T, fin), dtype=torch.bfloat16, device=device)
         st["dw"] = torch.empty((fout, fin), dtype=torch.float32, device=device)
-        st["ws_f"] = mxq.gemm_workspace(T, fout, fin, "e4m3", device)
-        st["ws_d"] = mxq.gemm_workspace(T, fin, fout, "e4m3", device)
-        st["ws_w"] = mxq.gemm_workspace(fout, fin, T, "e2m1", device)
         layers.append(st)
     return layers
 
 
-# kernels launched per layer: 3 dual quantizers, and 3 GEMMs each preceded
-# by one scale re-layout launch
-LAUNCHES_PER_LAYER = 3 + 3 * 2
+# The quantizers write their scales in the tensor cores' chunk layout and
+# the GEMMs read them in place, so each layer launches 3 dual quantizers and
+# 3 GEMMs (no scale re-layout pass, no GEMM workspace).
+SCALES = "tc"
+LAUNCHES_PER_LAYER = 3 + 3
 
 
 def run_layer(st, mark=None):
@@ -212,22 +213,22 @@ def run_layer(st, mark=None):
     T, fin, fout = st["L"]["T"], st["L"]["fin"], st["L"]["fout"]
     if mark:
         mark("q")
-    mxq.mx_quantize_dual(st["x"], "e4m3", False, "e2m1", True, out=st["xq"])
-    mxq.mx_quantize_dual(st["w"], "e4m3", False, "e4m3", False, out=st["wq"])
-    mxq.mx_quantize_dual(st["dy"], "e4m3", False, "e2m1", True, out=st["dyq"])
+    mxq.mx_quantize_dual(st["x"], "e4m3", False, "e2m1", True, out=st["xq"], scale_layout=SCALES)
+    mxq.mx_quantize_dual(st["w"], "e4m3", False, "e4m3", False, out=st["wq"], scale_layout=SCALES)
+    mxq.mx_quantize_dual(st["dy"], "e4m3", False, "e2m1", True, out=st["dyq"], scale_layout=SCALES)
     if mark:
         mark("f8")
     xr, sxr, xc, sxc = st["xq"]
     wr, swr, wc, swc = st["wq"]
     dr, sdr, dc, sdc = st["dyq"]
     mxq.mx_gemm(xr, sxr, wr, swr, "e4m3", T, fout, fin, torch.bfloat16, out=st["y"],
-                workspace=st["ws_f"])
+                scale_layout=SCALES)
     mxq.mx_gemm(dr, sdr, wc, swc, "e4m3", T, fin, fout, torch.bfloat16, out=st["dx"],
-                workspace=st["ws_d"])
+                scale_layout=SCALES)
     if mark:
         mark("f4")
     mxq.mx_gemm(dc, sdc, xc, sxc, "e2m1", fout, fin, T, torch.float32, out=st["dw"],
-                workspace=st["ws_w"])
+                scale_layout=SCALES)
 
 
 def run_step(layers, events=None):

@@ -83,6 +83,23 @@ typedef enum {
 
 typedef enum { MXQ_OUT_F32 = 0, MXQ_OUT_BF16 = 1 } mxq_out;
 
+/*
+ * Layout of the E8M0 scale bytes of a quantized operand with `lines` rows
+ * (output rows: rows for MXQ_ROWWISE, cols for MXQ_COLWISE_T) and a blocked
+ * dimension of `blocked` elements (32 per block):
+ *  MXQ_SCALES_ROWMAJOR: [lines][blocked / 32] bytes.
+ *  MXQ_SCALES_TC: the layout the tensor cores read the block scales in
+ *    (tcgen05.cp 32x128b.warpx4): 512-byte chunks, one per 128 lines x 4
+ *    blocks; chunk (line / 128) * (blocked / 128) + block / 4 holds the
+ *    byte of (line, block) at (line % 32) * 16 + ((line % 128) / 32) * 4 +
+ *    block % 4.  Lines past the end of the last 128-line tile hold zeros.
+ *    Size: mxq_scales_tc_bytes().  Needs blocked % 128 == 0 (E4M3, E5M2)
+ *    or % 256 == 0 (E2M1, whole GEMM stages) and a 16-byte aligned buffer.
+ *    A GEMM given scales in this layout (mxq_gemm_ex) skips its scale
+ *    re-layout pass and needs no workspace.
+ */
+typedef enum { MXQ_SCALES_ROWMAJOR = 0, MXQ_SCALES_TC = 1 } mxq_scale_layout;
+
 /* Library version, (major << 16) | minor. */
 int mxq_version(void);
 
@@ -129,6 +146,23 @@ mxq_status mxq_quantize_dual(const void* x, int64_t rows, int64_t cols,
                              int fmt_r, int had_r, void* codes_r, uint8_t* scales_r,
                              int fmt_c, int had_c, void* codes_c, uint8_t* scales_c,
                              void* stream);
+
+/*
+ * mxq_quantize / mxq_hadamard_quantize (hadamard != 0) with the scales in
+ * the given mxq_scale_layout.  MXQ_SCALES_ROWMAJOR is exactly mxq_quantize.
+ */
+mxq_status mxq_quantize_ex(const void* x, int64_t rows, int64_t cols, int layout, int fmt,
+                           int hadamard, void* codes, uint8_t* scales, int scale_layout,
+                           void* stream);
+
+/* mxq_quantize_dual with both outputs' scales in the given mxq_scale_layout. */
+mxq_status mxq_quantize_dual_ex(const void* x, int64_t rows, int64_t cols,
+                                int fmt_r, int had_r, void* codes_r, uint8_t* scales_r,
+                                int fmt_c, int had_c, void* codes_c, uint8_t* scales_c,
+                                int scale_layout, void* stream);
+
+/* Bytes of an MXQ_SCALES_TC scale buffer (0 on bad arguments). */
+size_t mxq_scales_tc_bytes(int64_t lines, int64_t blocked);
 
 /*
  * Ablation quantizer: MX quantization with the randomness that [AMD-FP4] §01
@@ -205,6 +239,18 @@ mxq_status mxq_gemm_quantize(const void* A, const uint8_t* sA, const void* B, co
                              int fmt, int64_t M, int64_t N, int64_t K, int out_fmt,
                              void* out_codes, uint8_t* out_scales, void* workspace,
                              size_t workspace_bytes, void* stream);
+
+/*
+ * mxq_gemm with sA and sB in the given mxq_scale_layout.  With
+ * MXQ_SCALES_TC (sA from an M-line, sB from an N-line quantization with
+ * blocked dimension K) the scale re-layout pass is skipped, workspace may be
+ * NULL and workspace_bytes 0, and K % 128 == 0 (E4M3, E5M2) or K % 256 == 0
+ * (E2M1) is required; sA and sB must be 16-byte aligned.
+ * MXQ_SCALES_ROWMAJOR is exactly mxq_gemm.
+ */
+mxq_status mxq_gemm_ex(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, int fmt,
+                       int64_t M, int64_t N, int64_t K, void* C, int out_dtype, int scale_layout,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace mxq_gemm needs for this problem (0 on bad arguments). */
 size_t mxq_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int fmt);

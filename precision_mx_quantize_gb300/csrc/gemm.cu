@@ -722,21 +722,26 @@ struct OutSpec {
 
 mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, int fmt,
                        int64_t M, int64_t N, int64_t K, const OutSpec& out, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+                       size_t workspace_bytes, void* stream, int scale_layout) {
   void* C = out.C;
   Plan p;
   if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
-  if (!A || !sA || !B || !sB || !C || !workspace) return MXQ_ERR_ARG;
+  if (scale_layout != MXQ_SCALES_ROWMAJOR && scale_layout != MXQ_SCALES_TC) return MXQ_ERR_ARG;
+  // scales already in the tensor-core chunk layout: no re-layout pass and
+  // no workspace; the chunks are read in place
+  const bool tc = scale_layout == MXQ_SCALES_TC;
+  if (!A || !sA || !B || !sB || !C || (!tc && !workspace)) return MXQ_ERR_ARG;
+  if (tc && K % (fmt == MXQ_E2M1 ? 256 : 128) != 0) return MXQ_ERR_ARG;
   if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
     return MXQ_ERR_ARG;
-  if (!aligned16(A) || !aligned16(B) || !aligned16(C) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return MXQ_ERR_ALIGN;
-  if (workspace_bytes < static_cast<size_t>(p.ws_a + p.ws_b)) return MXQ_ERR_WORKSPACE;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MXQ_ERR_ALIGN;
+  if (tc && (!aligned16(sA) || !aligned16(sB))) return MXQ_ERR_ALIGN;
+  if (!tc && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MXQ_ERR_ALIGN;
+  if (!tc && workspace_bytes < static_cast<size_t>(p.ws_a + p.ws_b)) return MXQ_ERR_WORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  {
+  if (!tc) {
     const int64_t total = (p.mp + p.np) * (p.kbp / 4);
     const int grid = static_cast<int>(std::min<int64_t>((total + 255) / 256, 4 * sm_count()));
     const SfSide sa{sA, M, p.mp, ws}, sb{sB, N, p.np, ws + p.ws_a};
@@ -767,18 +772,24 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
   }
 
   // Scale chunks as 2-D tensors of 512-byte rows (128 x uint32), one row per
-  // (128-row tile, k-chunk): a stage loads n_sfa consecutive rows.
+  // (128-row tile, k-chunk): a stage loads n_sfa consecutive rows.  The
+  // workspace holds chunks for the padded 256-row tiles; caller-provided
+  // chunks cover only the existing 128-row tiles, and loads of the missing
+  // ones read the zero fill.
   CUtensorMap tsa, tsb;
   {
     const int n_sfa = fmt == MXQ_E2M1 ? 2 : 1;
     const int64_t kcs = p.kbp / 4;
     for (int which = 0; which < 2; ++which) {
-      const int64_t rows = (which == 0 ? p.mp : p.np) / G_BM * kcs;
+      const int64_t lines = which == 0 ? (tc ? M : p.mp) : (tc ? N : p.np);
+      const int64_t rows = (lines + G_BM - 1) / G_BM * kcs;
+      const void* base = tc ? static_cast<const void*>(which == 0 ? sA : sB)
+                            : static_cast<const void*>(ws + (which == 0 ? 0 : p.ws_a));
       const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
       const cuuint64_t strides[1] = {512};
       const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(n_sfa)};
       if (encode(which == 0 ? &tsa : &tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
-                 ws + (which == 0 ? 0 : p.ws_a), dims, strides, box, estr,
+                 const_cast<void*>(base), dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return MXQ_ERR_CUDA;
@@ -820,8 +831,8 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
   }
   a.nk = static_cast<int32_t>((p.kbytes + G_BKB - 1) / G_BKB);
   a.kc_per_row = static_cast<int32_t>(p.kbp / 4);
-  a.sfa = ws;
-  a.sfb = ws + p.ws_a;
+  a.sfa = tc ? sA : ws;
+  a.sfb = tc ? sB : ws + p.ws_a;
   a.C = C;
   a.out_bf16 = out.kind == 1;
   a.out_q = out.kind == 2;
@@ -872,7 +883,21 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
   if (N % (out_dtype == MXQ_OUT_F32 ? 4 : 8) != 0) return MXQ_ERR_ALIGN;
   const OutSpec out{C, out_dtype == MXQ_OUT_BF16 ? 1 : 0, 0, nullptr};
-  return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream);
+  return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream,
+                     MXQ_SCALES_ROWMAJOR);
+}
+
+extern "C" mxq_status mxq_gemm_ex(const void* A, const uint8_t* sA, const void* B,
+                                  const uint8_t* sB, int fmt, int64_t M, int64_t N, int64_t K,
+                                  void* C, int out_dtype, int scale_layout, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (out_dtype != MXQ_OUT_F32 && out_dtype != MXQ_OUT_BF16) return MXQ_ERR_ARG;
+  Plan p;
+  if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
+  if (N % (out_dtype == MXQ_OUT_F32 ? 4 : 8) != 0) return MXQ_ERR_ALIGN;
+  const OutSpec out{C, out_dtype == MXQ_OUT_BF16 ? 1 : 0, 0, nullptr};
+  return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream,
+                     scale_layout);
 }
 
 extern "C" mxq_status mxq_gemm_quantize(const void* A, const uint8_t* sA, const void* B,
@@ -886,7 +911,8 @@ extern "C" mxq_status mxq_gemm_quantize(const void* A, const uint8_t* sA, const 
   if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
   if (N % 32 != 0) return MXQ_ERR_ARG;
   const OutSpec out{out_codes, 2, out_fmt, out_scales};
-  return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream);
+  return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream,
+                     MXQ_SCALES_ROWMAJOR);
 }
 
 // ---------------------------------------------------------------------------

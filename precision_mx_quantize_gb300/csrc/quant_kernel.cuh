@@ -66,6 +66,8 @@ struct QArgs {
   uint64_t timeout_ns;
   uint32_t sign_mask;         // ABL_SIGN: bit i negates element i of every block
   uint32_t seed_lo, seed_hi;  // ABL_SR: Philox key
+  int32_t sc_tc;              // scales in the GEMM's tensor-core chunk layout
+  int64_t kcs_r, kcs_c;       // chunks per 128-line tile of each output (tc layout)
 };
 
 template <int FMT>
@@ -444,6 +446,18 @@ MXQ_DEV void store_scales(const uint8_t* sc_tile, uint8_t* dst, int64_t n_lines,
   }
 }
 
+// Scale bytes of one tile in the tensor-core chunk layout the GEMM's
+// tcgen05.cp reads: a 128-line x 128-element tile has exactly one 512-byte
+// chunk (128 lines x 4 blocks), chunk (line0 / 128) * kcs + kc, with the 4
+// bytes of line i at (i % 32) * 16 + (i / 32) * 4.  Lines past the tensor
+// get zero scales, so the chunk never holds a stale or NaN byte.
+MXQ_DEV void store_scales_tc(const uint8_t* sc_tile, uint8_t* dst, int64_t n_lines, int64_t line0,
+                             int64_t kcs, int64_t kc, int i) {
+  uint8_t* chunk = dst + ((line0 >> 7) * kcs + kc) * 512;
+  const uint32_t w = line0 + i < n_lines ? *reinterpret_cast<const uint32_t*>(sc_tile + 4 * i) : 0u;
+  *reinterpret_cast<uint32_t*>(chunk + (i & 31) * 16 + (i >> 5) * 4) = w;
+}
+
 MXQ_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
@@ -524,13 +538,17 @@ __global__ void __launch_bounds__(Q_THREADS, 2)
       if (tn < a.n_tiles) issue(tn, s);
     }
     if constexpr (ROW) {
-      if (tid < Q_ROWS)
-        store_scales(sc_r, a.scales_r, a.R, R0, nsb_r, C0 >> 5, (a.C - C0 + 31) >> 5, tid);
+      if (tid < Q_ROWS) {
+        if (a.sc_tc) store_scales_tc(sc_r, a.scales_r, a.R, R0, a.kcs_r, C0 >> 7, tid);
+        else store_scales(sc_r, a.scales_r, a.R, R0, nsb_r, C0 >> 5, (a.C - C0 + 31) >> 5, tid);
+      }
     }
     if constexpr (COL) {
-      if (tid >= Q_THREADS - Q_COLS)
-        store_scales(sc_c, a.scales_c, a.C, C0, nsb_c, R0 >> 5, (a.R - R0 + 31) >> 5,
-                     tid - (Q_THREADS - Q_COLS));
+      if (tid >= Q_THREADS - Q_COLS) {
+        const int i = tid - (Q_THREADS - Q_COLS);
+        if (a.sc_tc) store_scales_tc(sc_c, a.scales_c, a.C, C0, a.kcs_c, R0 >> 7, i);
+        else store_scales(sc_c, a.scales_c, a.C, C0, nsb_c, R0 >> 5, (a.R - R0 + 31) >> 5, i);
+      }
     }
   }
   if (tid == 0) bulk_wait0();
@@ -560,7 +578,8 @@ bool valid_fmt(int f) { return f == MXQ_E4M3 || f == MXQ_E2M1 || f == MXQ_E5M2; 
 // as a persistent grid of up to 2 CTAs per SM.
 mxq_status quant_launch_k(QuantKernel k, const void* x, int64_t R, int64_t C, bool row, bool col,
                           int fr, void* codes_r, uint8_t* scales_r, int fc, void* codes_c,
-                          uint8_t* scales_c, uint32_t sign_mask, uint64_t seed, void* stream) {
+                          uint8_t* scales_c, uint32_t sign_mask, uint64_t seed, void* stream,
+                          int scale_layout = MXQ_SCALES_ROWMAJOR) {
   if (R < 0 || C < 0) return MXQ_ERR_ARG;
   if (R == 0 || C == 0) return MXQ_OK;
   if (R >= (int64_t(1) << 31) || C >= (int64_t(1) << 31)) return MXQ_ERR_ARG;
@@ -571,6 +590,15 @@ mxq_status quant_launch_k(QuantKernel k, const void* x, int64_t R, int64_t C, bo
   if (col && (R % 32 != 0 || C % 8 != 0)) return MXQ_ERR_ARG;
   if (!aligned16(x) || (row && !aligned16(codes_r)) || (col && !aligned16(codes_c)))
     return MXQ_ERR_ALIGN;
+  if (scale_layout != MXQ_SCALES_ROWMAJOR && scale_layout != MXQ_SCALES_TC) return MXQ_ERR_ARG;
+  const bool tc = scale_layout == MXQ_SCALES_TC;
+  if (tc) {
+    // whole chunks only: the blocked dimension covers whole 128-element
+    // chunks, and whole chunk pairs (one E2M1 GEMM stage) for E2M1
+    if (row && C % (fr == MXQ_E2M1 ? 256 : 128) != 0) return MXQ_ERR_ARG;
+    if (col && R % (fc == MXQ_E2M1 ? 256 : 128) != 0) return MXQ_ERR_ARG;
+    if ((row && !aligned16(scales_r)) || (col && !aligned16(scales_c))) return MXQ_ERR_ALIGN;
+  }
 
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
   if (!encode) return MXQ_ERR_CUDA;
@@ -619,6 +647,9 @@ mxq_status quant_launch_k(QuantKernel k, const void* x, int64_t R, int64_t C, bo
   a.sign_mask = sign_mask;
   a.seed_lo = static_cast<uint32_t>(seed);
   a.seed_hi = static_cast<uint32_t>(seed >> 32);
+  a.sc_tc = tc ? 1 : 0;
+  a.kcs_r = C / 128;
+  a.kcs_c = R / 128;
 
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM) != cudaSuccess)

@@ -184,9 +184,9 @@ QuantKernel pick(bool row, bool col, int fr, int hr, int fc, int hc) {
 
 mxq_status quant_launch(const void* x, int64_t R, int64_t C, bool row, bool col, int fr, int hr,
                         void* codes_r, uint8_t* scales_r, int fc, int hc, void* codes_c,
-                        uint8_t* scales_c, void* stream) {
+                        uint8_t* scales_c, void* stream, int scale_layout = MXQ_SCALES_ROWMAJOR) {
   return quant_launch_k(pick(row, col, fr, hr ? 1 : 0, fc, hc ? 1 : 0), x, R, C, row, col, fr,
-                        codes_r, scales_r, fc, codes_c, scales_c, 0u, 0u, stream);
+                        codes_r, scales_r, fc, codes_c, scales_c, 0u, 0u, stream, scale_layout);
 }
 
 }  // namespace
@@ -222,6 +222,31 @@ extern "C" mxq_status mxq_quantize_dual(const void* x, int64_t rows, int64_t col
   if (fmt_r == MXQ_E5M2 || fmt_c == MXQ_E5M2) return MXQ_ERR_UNSUPPORTED;
   return quant_launch(x, rows, cols, true, true, fmt_r, had_r != 0, codes_r, scales_r, fmt_c,
                       had_c != 0, codes_c, scales_c, stream);
+}
+
+extern "C" mxq_status mxq_quantize_ex(const void* x, int64_t rows, int64_t cols, int layout,
+                                      int fmt, int hadamard, void* codes, uint8_t* scales,
+                                      int scale_layout, void* stream) {
+  if (layout != MXQ_ROWWISE && layout != MXQ_COLWISE_T) return MXQ_ERR_ARG;
+  const bool row = layout == MXQ_ROWWISE;
+  const int h = hadamard != 0;
+  return quant_launch(x, rows, cols, row, !row, fmt, h, codes, scales, fmt, h, codes, scales,
+                      stream, scale_layout);
+}
+
+extern "C" mxq_status mxq_quantize_dual_ex(const void* x, int64_t rows, int64_t cols, int fmt_r,
+                                           int had_r, void* codes_r, uint8_t* scales_r,
+                                           int fmt_c, int had_c, void* codes_c,
+                                           uint8_t* scales_c, int scale_layout, void* stream) {
+  if (rows % 32 != 0 || cols % 32 != 0) return MXQ_ERR_ARG;
+  if (fmt_r == MXQ_E5M2 || fmt_c == MXQ_E5M2) return MXQ_ERR_UNSUPPORTED;
+  return quant_launch(x, rows, cols, true, true, fmt_r, had_r != 0, codes_r, scales_r, fmt_c,
+                      had_c != 0, codes_c, scales_c, stream, scale_layout);
+}
+
+extern "C" size_t mxq_scales_tc_bytes(int64_t lines, int64_t blocked) {
+  if (lines <= 0 || blocked <= 0 || blocked % 128 != 0) return 0;
+  return static_cast<size_t>((lines + 127) / 128) * static_cast<size_t>(blocked / 128) * 512u;
 }
 
 extern "C" mxq_status mxq_dequantize(const void* codes, const uint8_t* scales, int64_t rows,

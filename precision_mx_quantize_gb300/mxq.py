@@ -23,6 +23,9 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmxq.so")
 
 E4M3, E2M1, E5M2 = 0, 1, 2
 ROWWISE, COLWISE_T = 0, 1
+SCALES_ROWMAJOR, SCALES_TC = 0, 1
+SCALE_LAYOUTS = {"rowmajor": SCALES_ROWMAJOR, "tc": SCALES_TC,
+                 SCALES_ROWMAJOR: SCALES_ROWMAJOR, SCALES_TC: SCALES_TC}
 OUT_F32, OUT_BF16 = 0, 1
 FMTS = {"e4m3": E4M3, "e2m1": E2M1, "e5m2": E5M2, E4M3: E4M3, E2M1: E2M1, E5M2: E5M2}
 AXES = {"row": ROWWISE, "col": COLWISE_T, ROWWISE: ROWWISE, COLWISE_T: COLWISE_T}
@@ -38,6 +41,10 @@ SIGNATURES = [
     ("mxq_quantize", _I, [_P, _I64, _I64, _I, _I, _P, _P, _P]),
     ("mxq_hadamard_quantize", _I, [_P, _I64, _I64, _I, _I, _P, _P, _P]),
     ("mxq_quantize_dual", _I, [_P, _I64, _I64, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
+    ("mxq_quantize_ex", _I, [_P, _I64, _I64, _I, _I, _I, _P, _P, _I, _P]),
+    ("mxq_quantize_dual_ex", _I, [_P, _I64, _I64, _I, _I, _P, _P, _I, _I, _P, _P, _I, _P]),
+    ("mxq_scales_tc_bytes", _SZ, [_I64, _I64]),
+    ("mxq_gemm_ex", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _I, _P, _SZ, _P]),
     ("mxq_quantize_ablation", _I, [_P, _I64, _I64, _I, _I, _I, ctypes.c_uint32, _I, _U64, _P, _P, _P]),
     ("mxq_dequantize", _I, [_P, _P, _I64, _I64, _I, _I, _P, _I, _P]),
     ("mxq_gemm", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P, _SZ, _P]),
@@ -107,6 +114,27 @@ def mxq_quantize_dual(x, rows, cols, fmt_r, had_r, codes_r, scales_r, fmt_c, had
                                    codes_c, scales_c, stream)
 
 
+def mxq_quantize_ex(x, rows, cols, layout, fmt, hadamard, codes, scales, scale_layout, stream):
+    return lib().mxq_quantize_ex(x, rows, cols, layout, fmt, hadamard, codes, scales, scale_layout,
+                                 stream)
+
+
+def mxq_quantize_dual_ex(x, rows, cols, fmt_r, had_r, codes_r, scales_r, fmt_c, had_c, codes_c,
+                         scales_c, scale_layout, stream):
+    return lib().mxq_quantize_dual_ex(x, rows, cols, fmt_r, had_r, codes_r, scales_r, fmt_c,
+                                      had_c, codes_c, scales_c, scale_layout, stream)
+
+
+def mxq_scales_tc_bytes(lines, blocked):
+    return lib().mxq_scales_tc_bytes(lines, blocked)
+
+
+def mxq_gemm_ex(A, sA, B, sB, fmt, M, N, K, C, out_dtype, scale_layout, workspace, ws_bytes,
+                stream):
+    return lib().mxq_gemm_ex(A, sA, B, sB, fmt, M, N, K, C, out_dtype, scale_layout, workspace,
+                             ws_bytes, stream)
+
+
 def mxq_quantize_ablation(x, rows, cols, layout, fmt, hadamard, sign_mask, stochastic, seed, codes,
                           scales, stream):
     return lib().mxq_quantize_ablation(x, rows, cols, layout, fmt, hadamard, sign_mask, stochastic,
@@ -158,43 +186,69 @@ def code_shape(rows: int, cols: int, axis, fmt):
     return (r, c // 2 if f == E2M1 else c), (r, c // 32)
 
 
-def _alloc_codes(x, axis, fmt):
+def _alloc_codes(x, axis, fmt, scale_layout="rowmajor"):
     cs, ss = code_shape(x.shape[0], x.shape[1], axis, fmt)
+    if SCALE_LAYOUTS[scale_layout] == SCALES_TC:
+        lines, blocked = (x.shape[0], x.shape[1]) if AXES[axis] == ROWWISE else (x.shape[1], x.shape[0])
+        n = mxq_scales_tc_bytes(lines, blocked)
+        if n == 0:
+            raise ValueError(f"no tensor-core scale layout for {lines} lines x {blocked}")
+        ss = (n,)
     return (torch.empty(cs, dtype=torch.uint8, device=x.device),
             torch.empty(ss, dtype=torch.uint8, device=x.device))
 
 
-def mx_quantize(x: torch.Tensor, axis="row", fmt="e4m3", out=None):
-    """MX-quantize a contiguous bf16 CUDA tensor [rows, cols]; returns (codes, scales)."""
+def mx_quantize(x: torch.Tensor, axis="row", fmt="e4m3", out=None, scale_layout="rowmajor"):
+    """MX-quantize a contiguous bf16 CUDA tensor [rows, cols]; returns (codes, scales).
+
+    scale_layout "tc": scales in the tensor cores' chunk layout (a flat byte
+    tensor), which mx_gemm(..., scale_layout="tc") reads in place."""
     assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
-    codes, scales = out if out is not None else _alloc_codes(x, axis, fmt)
-    _ok(mxq_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
-                     codes.data_ptr(), scales.data_ptr(), _stream(x.device)), "mxq_quantize")
+    codes, scales = out if out is not None else _alloc_codes(x, axis, fmt, scale_layout)
+    if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
+        _ok(mxq_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
+                         codes.data_ptr(), scales.data_ptr(), _stream(x.device)), "mxq_quantize")
+    else:
+        _ok(mxq_quantize_ex(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt], 0,
+                            codes.data_ptr(), scales.data_ptr(), SCALES_TC, _stream(x.device)),
+            "mxq_quantize_ex")
     return codes, scales
 
 
-def hadamard_mx_quantize(x: torch.Tensor, axis="col", fmt="e2m1", out=None):
+def hadamard_mx_quantize(x: torch.Tensor, axis="col", fmt="e2m1", out=None,
+                         scale_layout="rowmajor"):
     """Fixed 32-point Hadamard rotation of each block, then MX quantization."""
     assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
-    codes, scales = out if out is not None else _alloc_codes(x, axis, fmt)
-    _ok(mxq_hadamard_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
-                              codes.data_ptr(), scales.data_ptr(), _stream(x.device)),
-        "mxq_hadamard_quantize")
+    codes, scales = out if out is not None else _alloc_codes(x, axis, fmt, scale_layout)
+    if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
+        _ok(mxq_hadamard_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
+                                  codes.data_ptr(), scales.data_ptr(), _stream(x.device)),
+            "mxq_hadamard_quantize")
+    else:
+        _ok(mxq_quantize_ex(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt], 1,
+                            codes.data_ptr(), scales.data_ptr(), SCALES_TC, _stream(x.device)),
+            "mxq_quantize_ex")
     return codes, scales
 
 
 def mx_quantize_dual(x: torch.Tensor, fmt_r="e4m3", had_r=False, fmt_c="e2m1", had_c=True,
-                     out=None):
+                     out=None, scale_layout="rowmajor"):
     """One pass producing the row-wise and the column-wise (transposed) outputs."""
     assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
     if out is None:
-        cr, sr = _alloc_codes(x, "row", fmt_r)
-        cc, sc = _alloc_codes(x, "col", fmt_c)
+        cr, sr = _alloc_codes(x, "row", fmt_r, scale_layout)
+        cc, sc = _alloc_codes(x, "col", fmt_c, scale_layout)
     else:
         cr, sr, cc, sc = out
-    _ok(mxq_quantize_dual(x.data_ptr(), x.shape[0], x.shape[1], FMTS[fmt_r], int(had_r),
-                          cr.data_ptr(), sr.data_ptr(), FMTS[fmt_c], int(had_c), cc.data_ptr(),
-                          sc.data_ptr(), _stream(x.device)), "mxq_quantize_dual")
+    if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
+        _ok(mxq_quantize_dual(x.data_ptr(), x.shape[0], x.shape[1], FMTS[fmt_r], int(had_r),
+                              cr.data_ptr(), sr.data_ptr(), FMTS[fmt_c], int(had_c), cc.data_ptr(),
+                              sc.data_ptr(), _stream(x.device)), "mxq_quantize_dual")
+    else:
+        _ok(mxq_quantize_dual_ex(x.data_ptr(), x.shape[0], x.shape[1], FMTS[fmt_r], int(had_r),
+                                 cr.data_ptr(), sr.data_ptr(), FMTS[fmt_c], int(had_c),
+                                 cc.data_ptr(), sc.data_ptr(), SCALES_TC, _stream(x.device)),
+            "mxq_quantize_dual_ex")
     return cr, sr, cc, sc
 
 
@@ -228,11 +282,19 @@ def gemm_workspace(M, N, K, fmt, device):
     return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
 
 
-def mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=torch.float32, out=None, workspace=None):
-    """C[M, N] = dec(A) @ dec(B)^T on the tensor cores (A, B K-major MX codes)."""
+def mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=torch.float32, out=None, workspace=None,
+            scale_layout="rowmajor"):
+    """C[M, N] = dec(A) @ dec(B)^T on the tensor cores (A, B K-major MX codes).
+
+    scale_layout "tc": sA, sB in the tensor cores' chunk layout (no workspace)."""
     od = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    if SCALE_LAYOUTS[scale_layout] == SCALES_TC:
+        _ok(mxq_gemm_ex(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M, N,
+                        K, out.data_ptr(), od, SCALES_TC, None, 0, _stream(A.device)),
+            "mxq_gemm_ex")
+        return out
     if workspace is None:
         workspace = gemm_workspace(M, N, K, fmt, A.device)
     _ok(mxq_gemm(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M, N, K,

@@ -63,3 +63,11 @@ def test_argument_errors_return_before_device_work(lib):
     assert A(p, 64, 64, ROW, 9, 1, 0, 1, 7, p, p, None) == 1
     assert A(ctypes.c_void_p(16 * 1024 + 2), 64, 64, ROW, E4, 0, 0, 1, 7, p, p, None) == 2
     assert A(p, 0, 64, ROW, E4, 1, 0xFFFFFFFF, 1, 2 ** 64 - 1, p, p, None) == 0
+
+
+def test_tc_scale_buffer_sizes(lib):
+    assert mxq.mxq_scales_tc_bytes(128, 128) == 512
+    assert mxq.mxq_scales_tc_bytes(129, 256) == 2 * 2 * 512
+    assert mxq.mxq_scales_tc_bytes(8192, 4096) == 64 * 32 * 512 == 8192 * 4096 // 32
+    assert mxq.mxq_scales_tc_bytes(64, 96) == 0
+    assert mxq.mxq_scales_tc_bytes(0, 128) == 0

@@ -1,8 +1,9 @@
 """Parity of the decoder-block pass that bench.py times, at its full size.
 
 The four Llama-3.1-8B linear layers at 8192 tokens run through the same
-functions the benchmark uses (dual quantizers, forward / dgrad MXFP8 GEMMs
-with bf16 output, Hadamard-MXFP4 Wgrad with fp32 output).  The oracle
+functions the benchmark uses (dual quantizers writing their scales in the
+tensor cores' chunk layout, forward / dgrad MXFP8 GEMMs with bf16 output,
+Hadamard-MXFP4 Wgrad with fp32 output, all reading those scales in place).  The oracle
 quantizes only sampled rows and columns of the same bf16 inputs and
 computes those outputs in fp64; every sampled output must meet the GEMM
 bound (2e-4 * sum|ab|, plus 2^-8 |C| for bf16 outputs).
@@ -79,10 +80,24 @@ def test_block_pass_layer(block, layer):
     _close(got, ref, S, bf16=False)
 
     # the quantizer outputs the GEMMs consumed are the oracle's, bit for bit
+    # (scales in the tensor cores' chunk layout: byte (line, block) of chunk
+    # (line / 128) * (blocked / 128) + block / 4 at (line % 32) * 16 +
+    # ((line % 128) / 32) * 4 + block % 4)
     xr, sxr, xc, sxc = st["xq"]
     ec, es = O.mx_quantize(x[t_rows], "row", "e4m3")
     np.testing.assert_array_equal(to_np(xr[torch.from_numpy(t_rows).cuda()]), ec)
-    np.testing.assert_array_equal(to_np(sxr[torch.from_numpy(t_rows).cuda()]), es)
+    np.testing.assert_array_equal(_tc_rows(to_np(sxr), t_rows, fin), es)
     ec, es = O.hadamard_mx_quantize(np.ascontiguousarray(x[:, i_rows]), "col", "e2m1")
     np.testing.assert_array_equal(to_np(xc[torch.from_numpy(i_rows).cuda()]), ec)
-    np.testing.assert_array_equal(to_np(sxc[torch.from_numpy(i_rows).cuda()]), es)
+    np.testing.assert_array_equal(_tc_rows(to_np(sxc), i_rows, T), es)
+
+
+def _tc_rows(buf, lines, blocked):
+    """Row-major scales of the given lines, read out of a chunk-layout buffer."""
+    kcs = blocked // 128
+    out = np.zeros((len(lines), blocked // 32), np.uint8)
+    for i, line in enumerate(lines):
+        for b in range(blocked // 32):
+            chunk = (line // 128) * kcs + b // 4
+            out[i, b] = buf[chunk * 512 + (line % 32) * 16 + ((line % 128) // 32) * 4 + b % 4]
+    return out
