@@ -368,6 +368,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs exist before anyone signals the peer
   tc_fence_after();
+  griddep_wait();  // the previous kernel's writes (codes, scales) are visible
+  griddep_launch_dependents();
   const int cid = blockIdx.x / G_CLUSTER, ncl = gridDim.x / G_CLUSTER;
   const uint32_t tmem = *tmem_base_slot;
   const int n_tiles = a.n_tiles, nk = a.nk;
@@ -856,7 +858,7 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM) != cudaSuccess)
     return MXQ_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = G_CLUSTER;
   attr[0].val.clusterDim.y = 1;
@@ -867,6 +869,11 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int max_clusters = max_gemm_clusters(cfg);
+  // persistent grid (every cluster resident): it may start while the
+  // previous kernel on the stream drains, and waits for it in the kernel
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   if (max_clusters <= 0) return MXQ_ERR_CUDA;
   cfg.gridDim = dim3(static_cast<unsigned>(G_CLUSTER * std::min(a.n_tiles, max_clusters)), 1, 1);
   if (cudaLaunchKernelEx(&cfg, mx_gemm_kernel, ta, tb, tsa, tsb, a) != cudaSuccess) return MXQ_ERR_CUDA;

@@ -112,6 +112,19 @@ MXQ_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---- programmatic dependent launch --------------------------------------------
+// Kernels launched with programmatic stream serialization may start while
+// the previous kernel on the stream is still finishing.  Each such kernel
+// sets up what needs no global memory (barriers, tensor memory, descriptor
+// prefetch), then waits for the previous grid to complete and its writes to
+// be visible before touching global memory, and lets the next kernel launch
+// early.  Every CTA of these grids is resident at once, so a dependent grid
+// waiting on free SMs can never hold up this one.
+MXQ_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MXQ_DEV void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- shared exponents -------------------------------------------------------
 // E8M0 byte from the magnitude bits of the block amax (fp32 layout):
 // floor(log2 amax) - emax + 127 = biased_exponent - emax, clamped at 0

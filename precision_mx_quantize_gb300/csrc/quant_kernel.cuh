@@ -491,6 +491,8 @@ __global__ void __launch_bounds__(Q_THREADS, 2)
     fence_mbar_init();
   }
   __syncthreads();
+  griddep_wait();               // the previous kernel's writes are visible
+  griddep_launch_dependents();
 
   auto issue = [&](int t, int s) {
     const int rt = t / a.n_ct, ct = t - rt * a.n_ct;
@@ -654,8 +656,20 @@ mxq_status quant_launch_k(QuantKernel k, const void* x, int64_t R, int64_t C, bo
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM) != cudaSuccess)
     return MXQ_ERR_CUDA;
+  // persistent grid (every CTA resident), launched so that it may start
+  // while the previous kernel on the stream drains
   const int grid = static_cast<int>(std::min<int64_t>(a.n_tiles, int64_t(2) * sm_count()));
-  k<<<grid, Q_THREADS, Q_SMEM, static_cast<cudaStream_t>(stream)>>>(map, map_r, map_c, a);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(Q_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Q_SMEM;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k, map, map_r, map_c, a) != cudaSuccess) return MXQ_ERR_CUDA;
   return launch_status();
 }
 
