@@ -252,6 +252,20 @@ mxq_status mxq_gemm_ex(const void* A, const uint8_t* sA, const void* B, const ui
                        int64_t M, int64_t N, int64_t K, void* C, int out_dtype, int scale_layout,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * mxq_gemm_quantize with the input scales sA, sB in scale_layout and the
+ * output scales in out_scale_layout (mxq_scale_layout).  With
+ * out_scale_layout MXQ_SCALES_TC the output (M lines, blocked dimension N)
+ * can feed mxq_gemm_ex directly; it needs N % 128 == 0 (E4M3, E5M2) or
+ * N % 256 == 0 (E2M1) and a 16-byte aligned out_scales of
+ * mxq_scales_tc_bytes(M, N) bytes.  Input-side rules as mxq_gemm_ex.
+ */
+mxq_status mxq_gemm_quantize_ex(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                                int fmt, int64_t M, int64_t N, int64_t K, int scale_layout,
+                                int out_fmt, void* out_codes, uint8_t* out_scales,
+                                int out_scale_layout, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
 /* Bytes of workspace mxq_gemm needs for this problem (0 on bad arguments). */
 size_t mxq_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int fmt);
 

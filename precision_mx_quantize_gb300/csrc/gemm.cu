@@ -80,6 +80,7 @@ struct GArgs {
   int32_t q_fmt;                // their element format
   uint8_t* q_scales;            // their E8M0 scales [M][N/32]
   int32_t q_scale_words;        // scale rows are 4-byte aligned: one word per 4 blocks
+  int32_t q_scale_tc;           // output scales in the tensor cores' chunk layout
   uint64_t timeout_ns;
 };
 
@@ -302,6 +303,12 @@ MXQ_DEV void store_row_codes(const uint32_t (&v)[128], const GArgs& a, int64_t r
       }
       sw |= sc << (8 * b);
     }
+  }
+  if (a.q_scale_tc) {
+    // one word of chunk (row / 128, col0 / 128): N % 128 == 0, so nblk == 4
+    uint8_t* chunk = a.q_scales + ((row >> 7) * (int64_t(a.N) >> 7) + (col0 >> 7)) * 512;
+    *reinterpret_cast<uint32_t*>(chunk + (row & 31) * 16 + ((row & 127) >> 5) * 4) = sw;
+    return;
   }
   uint8_t* srow = a.q_scales + row * (int64_t(a.N) / 32) + col0 / 32;
   if (a.q_scale_words && nblk == 4) {
@@ -563,6 +570,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       tile_coords(t, a, mp, nt);
       const int64_t row = (int64_t(mp) * G_CLUSTER + rank) * G_BM + quad * 32 + lane;
       const int64_t col0 = int64_t(nt) * G_BN + colh * 128;
+      if (a.q_scale_tc && row >= a.M && row < ((int64_t(a.M) + 127) & ~int64_t(127)) &&
+          col0 < a.N) {
+        // lines past M inside the last 128-line tile: zero scales, as in
+        // every chunk-layout buffer
+        uint8_t* chunk = a.q_scales + ((row >> 7) * (int64_t(a.N) >> 7) + (col0 >> 7)) * 512;
+        *reinterpret_cast<uint32_t*>(chunk + (row & 31) * 16 + ((row & 127) >> 5) * 4) = 0u;
+      }
       if (row < a.M && col0 < a.N) {
         const int64_t ncols = (a.N - col0) < 128 ? (a.N - col0) : 128;
         if (a.out_q) {
@@ -720,6 +734,7 @@ struct OutSpec {
   int kind;            // 0: fp32, 1: bf16, 2: MX codes
   int q_fmt;
   uint8_t* q_scales;
+  int q_scale_layout;  // mxq_scale_layout of q_scales
 };
 
 mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, int fmt,
@@ -841,6 +856,7 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
   a.q_fmt = out.q_fmt;
   a.q_scales = out.q_scales;
   a.q_scale_words = (reinterpret_cast<uintptr_t>(out.q_scales) & 3u) == 0 && (N / 32) % 4 == 0;
+  a.q_scale_tc = out.kind == 2 && out.q_scale_layout == MXQ_SCALES_TC;
   a.fp4 = fmt == MXQ_E2M1;
   // kind::mxf8f6f4 element types: E4M3 = 0, E5M2 = 1; kind::mxf4: E2M1 = 1
   a.elem_code = fmt == MXQ_E4M3 ? 0 : 1;
@@ -889,7 +905,7 @@ extern "C" mxq_status mxq_gemm(const void* A, const uint8_t* sA, const void* B, 
   Plan p;
   if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
   if (N % (out_dtype == MXQ_OUT_F32 ? 4 : 8) != 0) return MXQ_ERR_ALIGN;
-  const OutSpec out{C, out_dtype == MXQ_OUT_BF16 ? 1 : 0, 0, nullptr};
+  const OutSpec out{C, out_dtype == MXQ_OUT_BF16 ? 1 : 0, 0, nullptr, MXQ_SCALES_ROWMAJOR};
   return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream,
                      MXQ_SCALES_ROWMAJOR);
 }
@@ -902,7 +918,7 @@ extern "C" mxq_status mxq_gemm_ex(const void* A, const uint8_t* sA, const void* 
   Plan p;
   if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
   if (N % (out_dtype == MXQ_OUT_F32 ? 4 : 8) != 0) return MXQ_ERR_ALIGN;
-  const OutSpec out{C, out_dtype == MXQ_OUT_BF16 ? 1 : 0, 0, nullptr};
+  const OutSpec out{C, out_dtype == MXQ_OUT_BF16 ? 1 : 0, 0, nullptr, MXQ_SCALES_ROWMAJOR};
   return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream,
                      scale_layout);
 }
@@ -917,9 +933,31 @@ extern "C" mxq_status mxq_gemm_quantize(const void* A, const uint8_t* sA, const 
   Plan p;
   if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
   if (N % 32 != 0) return MXQ_ERR_ARG;
-  const OutSpec out{out_codes, 2, out_fmt, out_scales};
+  const OutSpec out{out_codes, 2, out_fmt, out_scales, MXQ_SCALES_ROWMAJOR};
   return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream,
                      MXQ_SCALES_ROWMAJOR);
+}
+
+extern "C" mxq_status mxq_gemm_quantize_ex(const void* A, const uint8_t* sA, const void* B,
+                                           const uint8_t* sB, int fmt, int64_t M, int64_t N,
+                                           int64_t K, int scale_layout, int out_fmt,
+                                           void* out_codes, uint8_t* out_scales,
+                                           int out_scale_layout, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  if (out_fmt != MXQ_E4M3 && out_fmt != MXQ_E5M2 && out_fmt != MXQ_E2M1) return MXQ_ERR_ARG;
+  if (out_scale_layout != MXQ_SCALES_ROWMAJOR && out_scale_layout != MXQ_SCALES_TC)
+    return MXQ_ERR_ARG;
+  if (!out_scales) return MXQ_ERR_ARG;
+  Plan p;
+  if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
+  if (N % 32 != 0) return MXQ_ERR_ARG;
+  if (out_scale_layout == MXQ_SCALES_TC) {
+    if (N % (out_fmt == MXQ_E2M1 ? 256 : 128) != 0) return MXQ_ERR_ARG;
+    if (!aligned16(out_scales)) return MXQ_ERR_ALIGN;
+  }
+  const OutSpec out{out_codes, 2, out_fmt, out_scales, out_scale_layout};
+  return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream,
+                     scale_layout);
 }
 
 // ---------------------------------------------------------------------------

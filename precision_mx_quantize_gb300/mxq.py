@@ -49,6 +49,8 @@ SIGNATURES = [
     ("mxq_dequantize", _I, [_P, _P, _I64, _I64, _I, _I, _P, _I, _P]),
     ("mxq_gemm", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P, _SZ, _P]),
     ("mxq_gemm_quantize", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
+    ("mxq_gemm_quantize_ex", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P, _P, _I, _P, _SZ,
+                                  _P]),
     ("mxq_gemm_workspace_size", _SZ, [_I64, _I64, _I64, _I]),
     ("mxq_gemm_noalloc", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P]),
     ("mxq_check", _I, [_P]),
@@ -153,6 +155,12 @@ def mxq_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt, codes, scales, worksp
                       stream):
     return lib().mxq_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt, codes, scales, workspace,
                                    ws_bytes, stream)
+
+
+def mxq_gemm_quantize_ex(A, sA, B, sB, fmt, M, N, K, scale_layout, out_fmt, codes, scales,
+                         out_scale_layout, workspace, ws_bytes, stream):
+    return lib().mxq_gemm_quantize_ex(A, sA, B, sB, fmt, M, N, K, scale_layout, out_fmt, codes,
+                                      scales, out_scale_layout, workspace, ws_bytes, stream)
 
 
 def mxq_gemm_noalloc(A, sA, B, sB, fmt, M, N, K, C, out_dtype, stream):
@@ -303,18 +311,32 @@ def mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=torch.float32, out=None, works
     return out
 
 
-def mx_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt="e4m3", out=None, workspace=None):
+def mx_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt="e4m3", out=None, workspace=None,
+                     scale_layout="rowmajor", out_scale_layout="rowmajor"):
     """dec(A) @ dec(B)^T with the epilogue writing row-wise MX codes of the
     fp32 product (blocks of 32 along N); returns (codes, scales)."""
+    in_tc = SCALE_LAYOUTS[scale_layout] == SCALES_TC
+    out_tc = SCALE_LAYOUTS[out_scale_layout] == SCALES_TC
     if out is None:
         cs, ss = code_shape(M, N, "row", out_fmt)
+        if out_tc:
+            ss = (mxq_scales_tc_bytes(M, N),)
         out = (torch.empty(cs, dtype=torch.uint8, device=A.device),
                torch.empty(ss, dtype=torch.uint8, device=A.device))
     codes, scales = out
-    if workspace is None:
+    if not in_tc and not out_tc:
+        if workspace is None:
+            workspace = gemm_workspace(M, N, K, fmt, A.device)
+        _ok(mxq_gemm_quantize(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M,
+                              N, K, FMTS[out_fmt], codes.data_ptr(), scales.data_ptr(),
+                              workspace.data_ptr(), workspace.numel(), _stream(A.device)),
+            "mxq_gemm_quantize")
+        return codes, scales
+    if not in_tc and workspace is None:
         workspace = gemm_workspace(M, N, K, fmt, A.device)
-    _ok(mxq_gemm_quantize(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M, N,
-                          K, FMTS[out_fmt], codes.data_ptr(), scales.data_ptr(),
-                          workspace.data_ptr(), workspace.numel(), _stream(A.device)),
-        "mxq_gemm_quantize")
+    ws_ptr, ws_n = (None, 0) if in_tc else (workspace.data_ptr(), workspace.numel())
+    _ok(mxq_gemm_quantize_ex(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M,
+                             N, K, SCALE_LAYOUTS[scale_layout], FMTS[out_fmt], codes.data_ptr(),
+                             scales.data_ptr(), SCALE_LAYOUTS[out_scale_layout], ws_ptr, ws_n,
+                             _stream(A.device)), "mxq_gemm_quantize_ex")
     return codes, scales

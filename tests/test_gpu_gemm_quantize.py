@@ -208,3 +208,31 @@ def test_mlp_up_forward_epilogue_codes_full_size_sampled():
     # with K = 4096 and heavy cancellation the bound is wide next to the
     # E4M3 step, so fewer elements are decided uniquely
     check_epilogue_codes(got_c, got_s, ref, S, "e4m3", min_unique=0.5)
+
+
+@pytest.mark.parametrize("fmt_in,fmt_out", [("e4m3", "e4m3"), ("e2m1", "e2m1"), ("e4m3", "e2m1")])
+def test_epilogue_tc_scale_layouts_and_chaining(fmt_in, fmt_out):
+    # tensor-core scale layout on the input side and on the output side:
+    # the same codes, the same scales rearranged, and the output feeds the
+    # next GEMM in place with results bitwise equal to the row-major path
+    from tests.test_gpu_scales_tc import tc_from_rowmajor
+    M, N, K = 200, 512, 512
+    a, sA, b, sB = _integer_operands(M, N, K, fmt_in, seed=31)
+    dA, dB = _dev(a), _dev(b)
+    c_rm, s_rm = mxq.mx_gemm_quantize(dA, _dev(sA), dB, _dev(sB), fmt_in, M, N, K, out_fmt=fmt_out)
+    tA = _dev(tc_from_rowmajor(sA, M, K))
+    tB = _dev(tc_from_rowmajor(sB, N, K))
+    c_tc, s_tc = mxq.mx_gemm_quantize(dA, tA, dB, tB, fmt_in, M, N, K, out_fmt=fmt_out,
+                                      scale_layout="tc", out_scale_layout="tc")
+    mxq.check()
+    assert torch.equal(c_rm, c_tc)
+    np.testing.assert_array_equal(to_np(s_tc), tc_from_rowmajor(to_np(s_rm), M, N))
+    # next layer: Z = Y W2^T with Y the quantized product (K2 = N)
+    N2 = 256
+    w2 = synth.weight(N2, N, seed=5).cuda()
+    w_rm = mxq.mx_quantize(w2, "row", fmt_out)
+    w_tc = mxq.mx_quantize(w2, "row", fmt_out, scale_layout="tc")
+    z_rm = mxq.mx_gemm(c_rm, s_rm, *w_rm, fmt_out, M, N2, N)
+    z_tc = mxq.mx_gemm(c_tc, s_tc, *w_tc, fmt_out, M, N2, N, scale_layout="tc")
+    mxq.check()
+    assert torch.equal(z_rm, z_tc)

@@ -113,3 +113,17 @@ def test_tc_argument_errors():
     # row-major through the extended entry point still needs its workspace
     assert mxq.mxq_gemm_ex(p, p, p, p, mxq.E4M3, 128, 128, 128, p, 0, 0, None, 0, s) == 1
     mxq.check()
+
+
+def test_epilogue_tc_argument_errors():
+    t = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    p = t.data_ptr()
+    s = mxq._stream()
+    TC, RM = mxq.SCALES_TC, mxq.SCALES_ROWMAJOR
+    Q = mxq.mxq_gemm_quantize_ex
+    assert Q(p, p, p, p, 0, 128, 96, 128, TC, 0, p, p, TC, None, 0, s) == 1        # N % 128
+    assert Q(p, p, p, p, 0, 128, 128, 128, TC, 1, p, p, TC, None, 0, s) == 1       # E2M1: N % 256
+    assert Q(p, p, p, p, 0, 128, 128, 128, TC, 0, p, p + 4, TC, None, 0, s) == 2   # alignment
+    assert Q(p, p, p, p, 0, 128, 128, 128, TC, 0, p, p, 5, None, 0, s) == 1        # layout
+    assert Q(p, p, p, p, 0, 128, 128, 128, RM, 0, p, p, TC, None, 0, s) == 1       # needs workspace
+    mxq.check()
