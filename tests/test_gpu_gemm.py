@@ -65,6 +65,9 @@ SHAPES = [
     (200, 264, 160),    # ragged M, N and a partial K stage
     (64, 40, 96),       # smaller than one tile
     (384, 776, 2080),   # odd tile counts, many K stages, K tail
+    (1, 4, 32),         # degenerate: one row, four columns, one k-block
+    (3, 12, 64),        # a few rows and columns, one E2M1 MMA's worth of K
+    (257, 260, 4128),   # one row / four columns past a tile, K just past a stage
 ]
 
 
