@@ -825,10 +825,10 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
     // Raster: tiles run in groups of `group` panels of one operand (the
     // grouped one) while the group sweeps all panels of the other.  The
     // grouped panels are touched by every wave of the group and stay in L2
-    // (budget 40 MB); the swept operand streams from DRAM once per group.
+    // (budget 64 MB); the swept operand streams from DRAM once per group.
     // Modeled DRAM bytes: grouped_total + swept_total * n_groups; the
     // orientation and group size with the fewest bytes win.
-    const double l2_budget = 40.0 * (1 << 20);
+    const double l2_budget = 64.0 * (1 << 20);
     const double panel = double(2 * G_BM) * double(p.kbytes);
     const int g_fit = static_cast<int>(std::max(1.0, std::floor(l2_budget / panel)));
     const double a_bytes = double(p.mp) * p.kbytes, b_bytes = double(p.np) * p.kbytes;
