@@ -659,6 +659,161 @@ def ablation_error(tokens=16384, n_out=4096, n_in=4096, draws=8):
             "E2M1 column-wise along tokens", "variants": out}
 
 
+def _time_rotating(launches, reps=20, warm=5, graph=False):
+    """Average ms per launch over `reps` launches cycling through `launches`
+    (one closure per buffer set; the sets together exceed 2x L2, so each
+    launch reads its inputs from HBM), CUDA events on the current stream.
+
+    graph: capture the `reps` launches in a CUDA graph and time its replay,
+    which takes the host's per-call work out of the measurement."""
+    import torch
+    for i in range(warm):
+        launches[i % len(launches)]()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for i in range(reps):
+                    launches[i % len(launches)]()
+        torch.cuda.current_stream().wait_stream(s)
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+    e0.record()
+    for i in range(reps):
+        launches[i % len(launches)]()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def sweep():
+    """The measurement configurations besides the block pass, one JSON line each.
+
+    * round trip: 256x1024 N(0,1) with 1% x100 outliers, row-wise E4M3
+      quantize then dequantize to fp32 (latency-bound: reported in us);
+    * dual Hadamard E2M1: 8192x4096 activation, Hadamard + E2M1 along rows
+      and columns in one pass (GB/s);
+    * MLP up-projection forward GEMM 8192x14336x4096 MXFP8, fp32 out, and
+      the MLP Wgrad GEMM 14336x4096x16384 MXFP4 (Hadamard E2M1 operands),
+      fp32 out (TFLOP/s), with their quantizers;
+    * quantizer bandwidth sweep: n = 2^20 .. 2^28 elements as [n/4096][4096]
+      bf16 N(0,1), {E4M3, E2M1} x {row, col, dual} x {Hadamard off, on}.
+    Buffers rotate so that each launch reads from HBM.
+    """
+    import torch
+
+    from precision_mx_quantize_gb300 import mxq, synth
+    peaks = _peaks()
+    hbm = peaks["hbm_gbs"]
+    lines = []
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+        lines.append(d)
+
+    # round trip (latency-bound)
+    x = synth.quantize_dequantize_small()["x"].cuda()
+    c, sc = mxq.mx_quantize(x, "row", "e4m3")
+    out = torch.empty((256, 1024), dtype=torch.float32, device="cuda")
+    ms_q = _time_rotating([lambda: mxq.mx_quantize(x, "row", "e4m3", out=(c, sc))], reps=200)
+    ms_d = _time_rotating([lambda: mxq.mx_dequantize(c, sc, 256, 1024, "row", "e4m3", out=out)], reps=200)
+    emit({"config": "round trip 256x1024 E4M3", "quantize_us": round(ms_q * 1e3, 2),
+          "dequantize_us": round(ms_d * 1e3, 2)})
+
+    # dual Hadamard E2M1 on the 8192x4096 activation
+    x = synth.hadamard_dual_activation()["x"].cuda()
+    outs = [mxq.mx_quantize_dual(x, "e2m1", True, "e2m1", True) for _ in range(4)]
+    xs = [x] + [x.clone() for _ in range(3)]
+    ms = _time_rotating([lambda i=i: mxq.mx_quantize_dual(xs[i], "e2m1", True, "e2m1", True, out=outs[i])
+                         for i in range(4)])
+    b = quant_bytes(8192, 4096, "e2m1", "e2m1")
+    emit({"config": "dual Hadamard E2M1 8192x4096", "ms": round(ms, 4),
+          "GB/s": round(b / ms / 1e6, 1), "frac_of_hbm": round(b / ms / 1e6 / hbm, 3)})
+    del x, xs, outs
+
+    # MLP up-projection forward (MXFP8) and MLP Wgrad (MXFP4)
+    d = synth.mlp_up_forward()
+    x, w = d["x"].cuda(), d["w"].cuda()
+    A, sA = mxq.mx_quantize(x, "row", "e4m3", scale_layout="tc")
+    B, sB = mxq.mx_quantize(w, "col", "e4m3", scale_layout="tc")
+    C = torch.empty((8192, 14336), dtype=torch.float32, device="cuda")
+    ms = _time_rotating([lambda: mxq.mx_gemm(A, sA, B, sB, "e4m3", 8192, 14336, 4096, out=C,
+                                              scale_layout="tc")])
+    f = 2 * 8192 * 14336 * 4096
+    emit({"config": "MLP up forward 8192x14336x4096 MXFP8, fp32 out", "ms": round(ms, 4),
+          "TFLOP/s": round(f / ms / 1e9, 1),
+          "frac_of_peak": round(f / ms / 1e9 / (2 * peaks["bf16_sustained"]), 3)})
+    del d, x, w, A, B, C
+    d = synth.mlp_wgrad()
+    dy, x = d["dy"].cuda(), d["x"].cuda()
+    qa = lambda: mxq.hadamard_mx_quantize(dy, "col", "e2m1", scale_layout="tc")
+    A, sA = qa()
+    B, sB = mxq.hadamard_mx_quantize(x, "col", "e2m1", scale_layout="tc")
+    ms_q = _time_rotating([lambda: mxq.hadamard_mx_quantize(dy, "col", "e2m1", out=(A, sA),
+                                                            scale_layout="tc"),
+                           lambda: mxq.hadamard_mx_quantize(x, "col", "e2m1", out=(B, sB),
+                                                            scale_layout="tc")])
+    C = torch.empty((14336, 4096), dtype=torch.float32, device="cuda")
+    ms = _time_rotating([lambda: mxq.mx_gemm(A, sA, B, sB, "e2m1", 14336, 4096, 16384, out=C,
+                                              scale_layout="tc")])
+    f = 2 * 14336 * 4096 * 16384
+    qb = (16384 * 14336 + 16384 * 4096) * (2 + 0.5 + 1 / 32)
+    emit({"config": "MLP Wgrad 14336x4096x16384 MXFP4 (Hadamard E2M1), fp32 out", "ms": round(ms, 4),
+          "TFLOP/s": round(f / ms / 1e9, 1),
+          "frac_of_peak": round(f / ms / 1e9 / (6 * peaks["bf16_sustained"]), 3),
+          "quantizers_GB/s": round(qb / (2 * ms_q) / 1e6, 1)})
+    del d, dy, x, A, B, C
+    torch.cuda.empty_cache()
+
+    # quantizer bandwidth sweep
+    def qbytes_of(n, layout, fmt):
+        code = n if fmt == "e4m3" else n // 2
+        one = code + n // 32
+        return 2 * n + (2 * one if layout == "dual" else one)
+
+    for fmt in ("e4m3", "e2m1"):
+        for layout in ("row", "col", "dual"):
+            for had in (False, True):
+                for e in range(20, 29):
+                    n = 1 << e
+                    rows = n // 4096
+                    per_set = qbytes_of(n, layout, fmt)
+                    sets = max(1, min(64, -(-2 * L2_BYTES // per_set)))
+                    g = torch.Generator(device="cuda")
+                    g.manual_seed(e)
+                    xs = [torch.randn(rows, 4096, device="cuda", generator=g).to(torch.bfloat16)
+                          for _ in range(sets)]
+                    if layout == "dual":
+                        outs = [mxq.mx_quantize_dual(xx, fmt, had, fmt, had) for xx in xs]
+                        ls = [lambda i=i: mxq.mx_quantize_dual(xs[i], fmt, had, fmt, had, out=outs[i])
+                              for i in range(sets)]
+                    else:
+                        q = mxq.hadamard_mx_quantize if had else mxq.mx_quantize
+                        outs = [q(xx, layout, fmt) for xx in xs]
+                        ls = [lambda i=i: q(xs[i], layout, fmt, out=outs[i]) for i in range(sets)]
+                    ms_eager = _time_rotating(ls, reps=max(20, sets))
+                    ms = _time_rotating(ls, reps=max(20, sets), graph=True)
+                    gbs = per_set / ms / 1e6
+                    emit({"config": "quantizer sweep", "fmt": fmt, "layout": layout,
+                          "hadamard": had, "elements": n, "us": round(ms * 1e3, 2),
+                          "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 3),
+                          "us_eager": round(ms_eager * 1e3, 2),
+                          "timing": "CUDA graph of the launches (us_eager: launched one by one)"})
+                    del xs, outs, ls
+                    torch.cuda.empty_cache()
+    mxq.check()
+    return lines
+
+
 def run_case(name, timed=False):
     """Run one kernel case three times (for ncu captures of a single kernel).
 
@@ -751,7 +906,13 @@ def main():
                     help="run one kernel case (for ncu) and exit; ablate-error prints the "
                          "Wgrad error of the rotation / rounding variants")
     ap.add_argument("--timed", action="store_true", help="with --case: time the case's launches")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the round-trip, dual-Hadamard, MLP GEMM and quantizer-sweep "
+                         "configurations (one JSON line each) and exit")
     args = ap.parse_args()
+    if args.sweep:
+        sweep()
+        return
     if args.case:
         run_case(args.case, timed=args.timed)
         return
