@@ -774,6 +774,23 @@ def sweep():
     del d, dy, x, A, B, C
     torch.cuda.empty_cache()
 
+    # dequantizer bandwidth (16384 x 8192 codes -> fp32 / bf16)
+    for fmt in ("e4m3", "e2m1"):
+        for axis in ("row", "col"):
+            x = torch.randn(16384, 8192, device="cuda").to(torch.bfloat16)
+            c, sc = mxq.mx_quantize(x, axis, fmt)
+            for od, ob in ((torch.float32, 4), (torch.bfloat16, 2)):
+                out = torch.empty((16384, 8192), dtype=od, device="cuda")
+                ms = _time_rotating([lambda: mxq.mx_dequantize(c, sc, 16384, 8192, axis, fmt, od, out=out)],
+                                    graph=True)
+                n = 16384 * 8192
+                b = n * ((1 if fmt == "e4m3" else 0.5) + 1 / 32 + ob)
+                emit({"config": "dequantize 16384x8192", "fmt": fmt, "layout": axis,
+                      "out": str(od).replace("torch.", ""), "us": round(ms * 1e3, 2),
+                      "GB/s": round(b / ms / 1e6, 1), "frac_of_hbm": round(b / ms / 1e6 / hbm, 3)})
+            del x, c, sc, out
+    torch.cuda.empty_cache()
+
     # quantizer bandwidth sweep
     def qbytes_of(n, layout, fmt):
         code = n if fmt == "e4m3" else n // 2
