@@ -80,49 +80,100 @@ MXQ_DEV void decode16(const uint8_t* codes, int64_t e0, float scale, float (&f)[
   }
 }
 
-template <int FMT, bool BF16>
+// Row-wise codes [R][C] -> out [R][C].  Each thread step covers 32 bytes
+// of output (8 fp32 or 16 bf16 elements, inside one block), written with
+// one 256-bit store when the output is 32-byte aligned, so a warp's loads
+// and stores are contiguous.  IDX is the index type: 32-bit when R * C
+// fits, which keeps the row / column split cheap.
+// Decode 8 consecutive elements of one block starting at element e0.
+template <int FMT>
+MXQ_DEV void decode8(const uint8_t* codes, int64_t e0, float scale, float (&f)[16]) {
+  if constexpr (FMT != MXQ_E2M1) {
+    const uint2 w = *reinterpret_cast<const uint2*>(codes + e0);
+    const uint32_t ws[2] = {w.x, w.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 lo = FMT == MXQ_E4M3 ? e4m3x2_to_f32(ws[i] & 0xFFFFu) : e5m2x2_to_f32(ws[i] & 0xFFFFu);
+      const float2 hi = FMT == MXQ_E4M3 ? e4m3x2_to_f32(ws[i] >> 16) : e5m2x2_to_f32(ws[i] >> 16);
+      f[4 * i] = lo.x * scale; f[4 * i + 1] = lo.y * scale;
+      f[4 * i + 2] = hi.x * scale; f[4 * i + 3] = hi.y * scale;
+    }
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + e0 / 2);
+#pragma unroll
+    for (int bidx = 0; bidx < 4; ++bidx) {
+      const float2 q = e2m1x2_to_f32((w >> (8 * bidx)) & 0xFFu);
+      f[2 * bidx] = q.x * scale;
+      f[2 * bidx + 1] = q.y * scale;
+    }
+  }
+}
+
+// 256-bit store of eight 32-bit words (32-byte aligned address).
+MXQ_DEV void st_v8(void* p, const uint32_t (&q)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(q[0]),
+               "r"(q[1]), "r"(q[2]), "r"(q[3]), "r"(q[4]), "r"(q[5]), "r"(q[6]), "r"(q[7])
+               : "memory");
+}
+
+template <int FMT, bool BF16, typename IDX>
 __global__ void __launch_bounds__(256) mx_dequant_rows(const uint8_t* __restrict__ codes,
                                                        const uint8_t* __restrict__ scales,
-                                                       int64_t R, int64_t C, void* out) {
-  const int64_t n16 = R * C / 16;
-  const int64_t nsb = C >> 5;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t e0 = i * 16;
-    const int64_t r = e0 / C, c = e0 - r * C;
-    const float sc = scale_value(scales[r * nsb + (c >> 5)]);
+                                                       int64_t R64, int64_t C64, void* out,
+                                                       int wide) {
+  constexpr int V = BF16 ? 16 : 8;
+  const IDX C = static_cast<IDX>(C64);
+  const IDX nv = static_cast<IDX>(R64 * C64 / V);  // C % 32 == 0
+  const IDX nsb = C >> 5;
+  for (IDX i = IDX(blockIdx.x) * blockDim.x + threadIdx.x; i < nv; i += IDX(gridDim.x) * blockDim.x) {
+    const IDX e0 = i * V;
+    const IDX r = e0 / C, c = e0 - r * C;
+    const float sc = scale_value(scales[int64_t(r) * nsb + (c >> 5)]);
     float f[16];
-    decode16<FMT>(codes, e0, sc, f);
     if constexpr (BF16) {
-      uint32_t p[8];
+      decode16<FMT>(codes, int64_t(e0), sc, f);
+      uint32_t q[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
-        p[k] = *reinterpret_cast<const uint32_t*>(&b);
+        q[k] = *reinterpret_cast<const uint32_t*>(&b);
       }
-      uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + e0);
-      o[0] = make_uint4(p[0], p[1], p[2], p[3]);
-      o[1] = make_uint4(p[4], p[5], p[6], p[7]);
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + int64_t(e0);
+      if (wide) {
+        st_v8(o, q);
+      } else {
+        reinterpret_cast<uint4*>(o)[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        reinterpret_cast<uint4*>(o)[1] = make_uint4(q[4], q[5], q[6], q[7]);
+      }
     } else {
-      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + e0);
+      decode8<FMT>(codes, int64_t(e0), sc, f);
+      uint32_t q[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) o[k] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+      for (int k = 0; k < 8; ++k) q[k] = __float_as_uint(f[k]);
+      float* o = static_cast<float*>(out) + int64_t(e0);
+      if (wide) {
+        st_v8(o, q);
+      } else {
+        reinterpret_cast<uint4*>(o)[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        reinterpret_cast<uint4*>(o)[1] = make_uint4(q[4], q[5], q[6], q[7]);
+      }
     }
   }
 }
 
 // Column-wise (transposed) codes [C][R] back to out [R][C]: a CTA decodes a
-// 32-column x 128-row tile into shared memory and writes it row by row.
+// 64-column x 128-row tile into shared memory (one 32-element block per
+// thread) and writes it row by row, two adjacent columns per lane.
 template <int FMT, bool BF16>
-__global__ void __launch_bounds__(128) mx_dequant_cols(const uint8_t* __restrict__ codes,
+__global__ void __launch_bounds__(256) mx_dequant_cols(const uint8_t* __restrict__ codes,
                                                        const uint8_t* __restrict__ scales,
                                                        int64_t R, int64_t C, int64_t n_cb,
                                                        void* out) {
-  __shared__ float tile[128][33];
+  __shared__ float tile[128][65];
   const int64_t cb = blockIdx.x % n_cb, rb = blockIdx.x / n_cb;
-  const int64_t c0 = cb * 32, r0 = rb * 128;
+  const int64_t c0 = cb * 64, r0 = rb * 128;
   const int tid = threadIdx.x;
-  const int cc = tid & 31, b = tid >> 5;
+  const int cc = tid & 63, b = tid >> 6;
   const int64_t c = c0 + cc, rr = r0 + 32 * b;
   if (c < C && rr < R) {
     const int64_t col_bytes = FMT != MXQ_E2M1 ? R : R / 2;
@@ -138,13 +189,26 @@ __global__ void __launch_bounds__(128) mx_dequant_cols(const uint8_t* __restrict
   }
   __syncthreads();
   const int lane = tid & 31;
-  for (int k = tid >> 5; k < 128; k += 4) {
-    const int64_t r = r0 + k, col = c0 + lane;
-    if (r < R && col < C) {
-      if constexpr (BF16)
-        static_cast<__nv_bfloat16*>(out)[r * C + col] = __float2bfloat16_rn(tile[k][lane]);
-      else
-        static_cast<float*>(out)[r * C + col] = tile[k][lane];
+  const bool pairs = (C & 1) == 0;  // two adjacent outputs form an aligned vector
+  for (int k = tid >> 5; k < 128; k += 8) {
+    const int64_t r = r0 + k, col = c0 + 2 * lane;
+    if (r >= R || col >= C) continue;
+    const float a0 = tile[k][2 * lane], a1 = tile[k][2 * lane + 1];
+    if (pairs) {
+      if constexpr (BF16) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(a0, a1);
+        *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(out) + r * C + col) = v;
+      } else {
+        *reinterpret_cast<float2*>(static_cast<float*>(out) + r * C + col) = make_float2(a0, a1);
+      }
+    } else {
+      if constexpr (BF16) {
+        static_cast<__nv_bfloat16*>(out)[r * C + col] = __float2bfloat16_rn(a0);
+        if (col + 1 < C) static_cast<__nv_bfloat16*>(out)[r * C + col + 1] = __float2bfloat16_rn(a1);
+      } else {
+        static_cast<float*>(out)[r * C + col] = a0;
+        if (col + 1 < C) static_cast<float*>(out)[r * C + col + 1] = a1;
+      }
     }
   }
 }
@@ -264,32 +328,36 @@ extern "C" mxq_status mxq_dequantize(const void* codes, const uint8_t* scales, i
   const uint8_t* c8 = static_cast<const uint8_t*>(codes);
   if (layout == MXQ_ROWWISE) {
     if (cols % 32 != 0) return MXQ_ERR_ARG;
-    const int64_t n16 = rows * cols / 16;
-    const int grid = static_cast<int>(std::min<int64_t>((n16 + 255) / 256, int64_t(8) * sm_count()));
+    const int64_t nv = rows * cols / (bf ? 16 : 8);
+    const int grid = static_cast<int>(std::min<int64_t>((nv + 255) / 256, int64_t(8) * sm_count()));
+    const int wide = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+    // 32-bit indices while every element index and the grid stride fit
+    const bool small = rows * cols + int64_t(grid) * 256 * 16 < (int64_t(1) << 31);
+#define MXQ_DQ_ROWS(F_, B_)                                                                     \
+  (small ? (mx_dequant_rows<F_, B_, uint32_t><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out, wide), 0) \
+         : (mx_dequant_rows<F_, B_, int64_t><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out, wide), 0))
     if (fmt == MXQ_E4M3) {
-      if (bf) mx_dequant_rows<MXQ_E4M3, true><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
-      else mx_dequant_rows<MXQ_E4M3, false><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
+      if (bf) MXQ_DQ_ROWS(MXQ_E4M3, true); else MXQ_DQ_ROWS(MXQ_E4M3, false);
     } else if (fmt == MXQ_E5M2) {
-      if (bf) mx_dequant_rows<MXQ_E5M2, true><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
-      else mx_dequant_rows<MXQ_E5M2, false><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
+      if (bf) MXQ_DQ_ROWS(MXQ_E5M2, true); else MXQ_DQ_ROWS(MXQ_E5M2, false);
     } else {
-      if (bf) mx_dequant_rows<MXQ_E2M1, true><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
-      else mx_dequant_rows<MXQ_E2M1, false><<<grid, 256, 0, st>>>(c8, scales, rows, cols, out);
+      if (bf) MXQ_DQ_ROWS(MXQ_E2M1, true); else MXQ_DQ_ROWS(MXQ_E2M1, false);
     }
+#undef MXQ_DQ_ROWS
   } else {
     if (rows % 32 != 0) return MXQ_ERR_ARG;
-    const int64_t n_cb = (cols + 31) / 32, n_rb = (rows + 127) / 128;
+    const int64_t n_cb = (cols + 63) / 64, n_rb = (rows + 127) / 128;
     if (n_cb * n_rb >= (int64_t(1) << 31)) return MXQ_ERR_ARG;
     const int grid = static_cast<int>(n_cb * n_rb);
     if (fmt == MXQ_E4M3) {
-      if (bf) mx_dequant_cols<MXQ_E4M3, true><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
-      else mx_dequant_cols<MXQ_E4M3, false><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
+      if (bf) mx_dequant_cols<MXQ_E4M3, true><<<grid, 256, 0, st>>>(c8, scales, rows, cols, n_cb, out);
+      else mx_dequant_cols<MXQ_E4M3, false><<<grid, 256, 0, st>>>(c8, scales, rows, cols, n_cb, out);
     } else if (fmt == MXQ_E5M2) {
-      if (bf) mx_dequant_cols<MXQ_E5M2, true><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
-      else mx_dequant_cols<MXQ_E5M2, false><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
+      if (bf) mx_dequant_cols<MXQ_E5M2, true><<<grid, 256, 0, st>>>(c8, scales, rows, cols, n_cb, out);
+      else mx_dequant_cols<MXQ_E5M2, false><<<grid, 256, 0, st>>>(c8, scales, rows, cols, n_cb, out);
     } else {
-      if (bf) mx_dequant_cols<MXQ_E2M1, true><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
-      else mx_dequant_cols<MXQ_E2M1, false><<<grid, 128, 0, st>>>(c8, scales, rows, cols, n_cb, out);
+      if (bf) mx_dequant_cols<MXQ_E2M1, true><<<grid, 256, 0, st>>>(c8, scales, rows, cols, n_cb, out);
+      else mx_dequant_cols<MXQ_E2M1, false><<<grid, 256, 0, st>>>(c8, scales, rows, cols, n_cb, out);
     }
   }
   return launch_status();
