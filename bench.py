@@ -485,10 +485,31 @@ def e2e_measure(args, layers, flops, device):
     t1.record(compute)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
+    h2d_gbs, d2h_gbs = _link_probe(host_in[0]["x"], layers[0]["x"], host_out[0], layers[0]["dw"])
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "overlap": "H2D, compute and D2H on separate streams, ordered per layer by events"}
+            "overlap": "H2D, compute and D2H on separate streams, ordered per layer by events",
+            "link": {"h2d_GB/s": h2d_gbs, "d2h_GB/s": d2h_gbs,
+                     "h2d_bound_ms": round(h2d / (h2d_gbs * 1e6), 3),
+                     "note": "one pinned copy each way, measured on this box after the e2e steps"}}
+
+
+def _link_probe(h_in, d_in, h_out, d_out, reps=5):
+    """GB/s of plain pinned host->device and device->host copies on this machine."""
+    import torch
+    res = []
+    for dst, src in ((d_in, h_in), (h_out, d_out)):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        res.append(round(reps * src.numel() * src.element_size() / (e0.elapsed_time(e1) * 1e6), 1))
+    return res[0], res[1]
 
 
 # ---------------------------------------------------------------------------
