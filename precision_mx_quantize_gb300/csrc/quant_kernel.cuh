@@ -152,8 +152,11 @@ MXQ_DEV uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t k0, uint32_t k1) 
   uint32_t x0 = c0, x1 = c1, x2 = 0u, x3 = 0u;
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
-    const uint32_t lo0 = 0xD2511F53u * x0, hi0 = __umulhi(0xD2511F53u, x0);
-    const uint32_t lo1 = 0xCD9E8D57u * x2, hi1 = __umulhi(0xCD9E8D57u, x2);
+    // one 32x32 -> 64-bit multiply each gives both halves
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * x0;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * x2;
+    const uint32_t lo0 = static_cast<uint32_t>(p0), hi0 = static_cast<uint32_t>(p0 >> 32);
+    const uint32_t lo1 = static_cast<uint32_t>(p1), hi1 = static_cast<uint32_t>(p1 >> 32);
     x0 = hi1 ^ x1 ^ k0;
     x1 = lo1;
     x2 = hi0 ^ x3 ^ k1;
@@ -174,12 +177,21 @@ MXQ_DEV uint4 group_bits(uint64_t g, const QArgs& a) {
 // Stochastic rounding of one scaled element v onto the element grid.  With
 // k = max(floor(log2|v|), emin) the grid step at |v| is q = 2^(k - mbits);
 // t = |v| / q, F = floor(frac(t) * 2^32), and the magnitude becomes
-// (floor(t) + [r < F]) * q, saturated at the largest finite element.  Each
-// step is exact in fp32 (power-of-two scalings, floor, and the subtraction
-// of the floor), so the result lies on the grid and the round-to-nearest
-// conversion that follows encodes it unchanged.  The sign is kept.
+// (floor(t) + [r < F]) * q, saturated at the largest finite element.  The
+// sign is kept; the result lies on the grid, so the round-to-nearest
+// conversion that follows encodes it unchanged.
+//  - General form (sr_round_fp): every step is an exact fp32 operation on
+//    power-of-two scalings (multiply, floor, subtraction of the floor).
+//  - E4M3 / E5M2 fast path: for |v| >= 2^emin, q is one unit in bit
+//    23 - mbits of |v|'s fp32 pattern, so floor(t) * q is the pattern with
+//    the lower bits cleared, frac(t) * 2^32 is those lower bits shifted to
+//    the top of a word, and adding the unit rounds up (a carry into the
+//    exponent is the next binade's first grid point): integer work only.
+//    Values under 2^emin (rare for these formats) take the general form.
+//    E2M1 keeps the general form for all values: its subnormal range [0, 1)
+//    holds many scaled elements, and a divergent branch would cost more.
 template <int FMT>
-MXQ_DEV float sr_round(float v, uint32_t r) {
+MXQ_DEV float sr_round_fp(float v, uint32_t r) {
   const uint32_t b = __float_as_uint(v);
   const uint32_t sign = b & 0x80000000u;
   const float av = __uint_as_float(b ^ sign);
@@ -190,6 +202,23 @@ MXQ_DEV float sr_round(float v, uint32_t r) {
   const float m = (lo + (r < F ? 1.0f : 0.0f)) *
                   __uint_as_float(static_cast<uint32_t>(127 - Elem<FMT>::mbits + k) << 23);
   return __uint_as_float(__float_as_uint(fminf(m, Elem<FMT>::maxv)) | sign);
+}
+
+template <int FMT>
+MXQ_DEV float sr_round(float v, uint32_t r) {
+  if constexpr (FMT == MXQ_E2M1) {
+    return sr_round_fp<FMT>(v, r);
+  } else {
+    constexpr int MB = Elem<FMT>::mbits;
+    const uint32_t b = __float_as_uint(v);
+    const uint32_t sign = b & 0x80000000u;
+    const uint32_t a = b ^ sign;
+    if (static_cast<int>(a >> 23) - 127 < Elem<FMT>::emin) return sr_round_fp<FMT>(v, r);
+    const uint32_t unit = 1u << (23 - MB);
+    const uint32_t F = a << (9 + MB);
+    const uint32_t m = (a & ~(unit - 1u)) + (r < F ? unit : 0u);
+    return __uint_as_float(__float_as_uint(fminf(__uint_as_float(m), Elem<FMT>::maxv)) | sign);
+  }
 }
 
 // Quantize two 32-blocks held lane-wise in v.  For the unrotated path the
