@@ -206,3 +206,25 @@ def test_rotation_lowers_wgrad_error_on_outlier_columns():
     err0 = np.linalg.norm(plain - exact) / np.linalg.norm(exact)
     err1 = np.linalg.norm(rot - exact) / np.linalg.norm(exact)
     assert err1 < err0
+
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3", "float8_e4m3fn"), ("e5m2", "float8_e5m2")])
+def test_gemm_oracle_against_torch_fp8_decoding(fmt, tdt):
+    # an independent decode: torch's own fp8 dtypes read the code bytes, the
+    # block scales are applied as powers of two and a float64 matmul sums
+    import torch
+    rng = np.random.default_rng(17)
+    M, N, K = 24, 40, 96
+    table = O.decode_table(fmt)
+    finite = np.flatnonzero(np.isfinite(table)).astype(np.uint8)
+    A = rng.choice(finite, size=(M, K))
+    B = rng.choice(finite, size=(N, K))
+    sA = rng.integers(110, 140, size=(M, K // 32)).astype(np.uint8)
+    sB = rng.integers(110, 140, size=(N, K // 32)).astype(np.uint8)
+    ref, _ = O.mx_gemm_f64(A, sA, B, sB, fmt)
+    dt = getattr(torch, tdt)
+    a = torch.from_numpy(A).view(dt).to(torch.float64).numpy()
+    b = torch.from_numpy(B).view(dt).to(torch.float64).numpy()
+    a = a * np.exp2(np.repeat(sA.astype(np.float64) - 127, 32, axis=1))
+    b = b * np.exp2(np.repeat(sB.astype(np.float64) - 127, 32, axis=1))
+    np.testing.assert_array_equal(ref, a @ b.T)
