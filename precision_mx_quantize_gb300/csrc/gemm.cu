@@ -26,11 +26,16 @@
 //              lane;
 //   warps 2-9  (both CTAs) epilogue: each drains 32 accumulator lanes x 128
 //              columns into registers, tells the leader the accumulator is
-//              free, and stores its rows (256-bit stores when aligned) while
-//              the next tile's main loop runs.
-// The row-major scales are first rewritten (a small pre-pass kernel) into
-// the tensor-core chunk layout in the caller's workspace: for every 128-row
-// x 4-block chunk, byte (r % 32) * 16 + (r / 32) * 4 + (kb % 4).
+//              free (a relaxed arrive: it must not wait for earlier stores),
+//              and stores its rows -- fp32, bf16, or row-wise MX codes of the
+//              product -- paced over the next tile's main loop, with 256-bit
+//              stores when aligned.
+// Scales: tcgen05.cp reads them in a chunk layout (for every 128-row x
+// 4-block chunk, byte (r % 32) * 16 + (r / 32) * 4 + (kb % 4)).  Scales the
+// quantizers wrote in that layout are loaded in place; row-major scales are
+// first rewritten into it by a small pre-pass kernel in the caller's
+// workspace.  The kernel is launched with programmatic stream serialization
+// and waits for the previous grid (griddepcontrol) before any global access.
 #include <mutex>
 
 #include "mxq_common.cuh"

@@ -22,7 +22,10 @@
 // Codes go to a swizzled shared-memory staging tile that one TMA store per
 // layout writes out (the transposed column-wise tile included), so global
 // writes are whole-tile bulk copies; scales leave as one 4-byte word per
-// row or column of the tile.
+// row or column of the tile, either row-major or straight into the GEMM's
+// tensor-core chunk layout (a tile is exactly one 512-byte chunk).  The
+// grid is launched with programmatic stream serialization and waits for the
+// previous grid (griddepcontrol) before touching global memory.
 //
 // Ablation variants (template flag ABL): the same AMD FP4 page, §01, sets
 // its deterministic rotation against random Hadamard rotations and
