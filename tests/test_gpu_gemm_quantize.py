@@ -236,3 +236,22 @@ def test_epilogue_tc_scale_layouts_and_chaining(fmt_in, fmt_out):
     z_tc = mxq.mx_gemm(c_tc, s_tc, *w_tc, fmt_out, M, N2, N, scale_layout="tc")
     mxq.check()
     assert torch.equal(z_rm, z_tc)
+
+
+@pytest.mark.parametrize("in_layout,out_layout", [("rowmajor", "tc"), ("tc", "rowmajor")])
+def test_epilogue_mixed_scale_layouts(in_layout, out_layout):
+    from tests.test_gpu_scales_tc import tc_from_rowmajor
+    M, N, K = 136, 256, 512
+    a, sA, b, sB = _integer_operands(M, N, K, "e4m3", seed=41)
+    if in_layout == "tc":
+        sA, sB = tc_from_rowmajor(sA, M, K), tc_from_rowmajor(sB, N, K)
+    codes, scales = mxq.mx_gemm_quantize(_dev(a), _dev(sA), _dev(b), _dev(sB), "e4m3", M, N, K,
+                                         out_fmt="e4m3", scale_layout=in_layout,
+                                         out_scale_layout=out_layout)
+    mxq.check()
+    a2, sA2, b2, sB2 = _integer_operands(M, N, K, "e4m3", seed=41)
+    ref, _ = O.mx_gemm_f64(a2, sA2, b2, sB2, "e4m3")
+    ec, es = O.mx_quantize(ref.astype(np.float32), "row", "e4m3")
+    np.testing.assert_array_equal(to_np(codes), ec)
+    exp_s = tc_from_rowmajor(es, M, N) if out_layout == "tc" else es
+    np.testing.assert_array_equal(to_np(scales), exp_s)
