@@ -7,6 +7,8 @@
 // rotation before the MXFP4 quantization of the Wgrad operands;
 // "MindSpeed LLM FSDP2量化特性：低比特大模型训练完全指南", 第 1 步 -- block size
 // 32, E4M3 elements.  Bit-level rules: OCP MX v1.0 / OCP FP8.
+#include <type_traits>
+
 #include "quant_kernel.cuh"
 
 namespace mxq {
@@ -161,54 +163,70 @@ __global__ void __launch_bounds__(256) mx_dequant_rows(const uint8_t* __restrict
   }
 }
 
-// Column-wise (transposed) codes [C][R] back to out [R][C]: a CTA decodes a
-// 64-column x 128-row tile into shared memory (one 32-element block per
-// thread) and writes it row by row, two adjacent columns per lane.
+// Column-wise (transposed) codes [C][R] back to out [R][C].  A CTA decodes a
+// TR-row x TC-column tile into shared memory, already converted to the
+// output type (one 32-element block per thread), and writes it row by row,
+// TC / 32 adjacent outputs per lane in one vector store.  Tiles: 64 x 128
+// for bf16 output (8-byte stores, 256 bytes per warp and row), 64 x 64 for
+// fp32 (8-byte stores); both keep the tile at 17 KB, so many CTAs stay
+// resident and their code loads overlap.
+template <int FMT, bool BF16>
+struct DqColsTile {
+  static constexpr int TR = 64, TC = BF16 ? 128 : 64;
+};
+
 template <int FMT, bool BF16>
 __global__ void __launch_bounds__(256) mx_dequant_cols(const uint8_t* __restrict__ codes,
                                                        const uint8_t* __restrict__ scales,
                                                        int64_t R, int64_t C, int64_t n_cb,
                                                        void* out) {
-  __shared__ float tile[128][65];
+  using OutT = typename std::conditional<BF16, __nv_bfloat16, float>::type;
+  constexpr int TR = DqColsTile<FMT, BF16>::TR, TC = DqColsTile<FMT, BF16>::TC;
+  constexpr int LD = TC + 16 / int(sizeof(OutT));  // row pitch: 16-byte padding
+  constexpr int V = TC / 32;                         // outputs per lane and row
+  constexpr int VB = V * int(sizeof(OutT));          // bytes per lane and row
+  static_assert(VB == 8 && (LD * sizeof(OutT)) % VB == 0, "lane vectors stay aligned");
+  __shared__ __align__(16) OutT tile[TR * LD];
   const int64_t cb = blockIdx.x % n_cb, rb = blockIdx.x / n_cb;
-  const int64_t c0 = cb * 64, r0 = rb * 128;
-  const int tid = threadIdx.x;
-  const int cc = tid & 63, b = tid >> 6;
-  const int64_t c = c0 + cc, rr = r0 + 32 * b;
-  if (c < C && rr < R) {
-    const int64_t col_bytes = FMT != MXQ_E2M1 ? R : R / 2;
+  const int64_t c0 = cb * TC, r0 = rb * TR;
+  const int64_t col_bytes = FMT != MXQ_E2M1 ? R : R / 2;
+  constexpr int NB = TC * (TR / 32);                 // blocks in the tile
+  for (int blk = threadIdx.x; blk < NB; blk += 256) {
+    const int cc = blk % TC, b = blk / TC;
+    const int64_t c = c0 + cc, rr = r0 + 32 * b;
+    if (c >= C || rr >= R) continue;
     const float sc = scale_value(scales[c * (R >> 5) + (rr >> 5)]);
     const uint8_t* src = codes + c * col_bytes;
-    float f[16];
+    float f[16], g[16];
     decode16<FMT>(src, rr, sc, f);
+    decode16<FMT>(src, rr + 16, sc, g);
+    OutT* t = tile + (32 * b) * LD + cc;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) tile[32 * b + j][cc] = f[j];
-    decode16<FMT>(src, rr + 16, sc, f);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) tile[32 * b + 16 + j][cc] = f[j];
+    for (int j = 0; j < 16; ++j) {
+      if constexpr (BF16) {
+        t[j * LD] = __float2bfloat16_rn(f[j]);
+        t[(16 + j) * LD] = __float2bfloat16_rn(g[j]);
+      } else {
+        t[j * LD] = f[j];
+        t[(16 + j) * LD] = g[j];
+      }
+    }
   }
   __syncthreads();
-  const int lane = tid & 31;
-  const bool pairs = (C & 1) == 0;  // two adjacent outputs form an aligned vector
-  for (int k = tid >> 5; k < 128; k += 8) {
-    const int64_t r = r0 + k, col = c0 + 2 * lane;
-    if (r >= R || col >= C) continue;
-    const float a0 = tile[k][2 * lane], a1 = tile[k][2 * lane + 1];
-    if (pairs) {
-      if constexpr (BF16) {
-        const __nv_bfloat162 v = __floats2bfloat162_rn(a0, a1);
-        *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(out) + r * C + col) = v;
-      } else {
-        *reinterpret_cast<float2*>(static_cast<float*>(out) + r * C + col) = make_float2(a0, a1);
-      }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t col = c0 + V * lane;
+  if (col >= C) return;
+  const bool vec = C % V == 0;  // then a lane's V outputs are all inside the row, aligned
+  for (int k = warp; k < TR; k += 8) {
+    const int64_t r = r0 + k;
+    if (r >= R) break;
+    const OutT* s = tile + k * LD + V * lane;
+    OutT* d = static_cast<OutT*>(out) + r * C + col;
+    if (vec) {
+      *reinterpret_cast<uint2*>(d) = *reinterpret_cast<const uint2*>(s);
     } else {
-      if constexpr (BF16) {
-        static_cast<__nv_bfloat16*>(out)[r * C + col] = __float2bfloat16_rn(a0);
-        if (col + 1 < C) static_cast<__nv_bfloat16*>(out)[r * C + col + 1] = __float2bfloat16_rn(a1);
-      } else {
-        static_cast<float*>(out)[r * C + col] = a0;
-        if (col + 1 < C) static_cast<float*>(out)[r * C + col + 1] = a1;
-      }
+      for (int v = 0; v < V; ++v)
+        if (col + v < C) d[v] = s[v];
     }
   }
 }
@@ -346,7 +364,8 @@ extern "C" mxq_status mxq_dequantize(const void* codes, const uint8_t* scales, i
 #undef MXQ_DQ_ROWS
   } else {
     if (rows % 32 != 0) return MXQ_ERR_ARG;
-    const int64_t n_cb = (cols + 63) / 64, n_rb = (rows + 127) / 128;
+    const int tr = 64, tc = bf ? DqColsTile<0, true>::TC : DqColsTile<0, false>::TC;
+    const int64_t n_cb = (cols + tc - 1) / tc, n_rb = (rows + tr - 1) / tr;
     if (n_cb * n_rb >= (int64_t(1) << 31)) return MXQ_ERR_ARG;
     const int grid = static_cast<int>(n_cb * n_rb);
     if (fmt == MXQ_E4M3) {

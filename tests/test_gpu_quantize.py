@@ -156,6 +156,25 @@ def test_dequantize_arbitrary_scales():
     np.testing.assert_array_equal(to_np(got3), exp3)
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("shape", [(32, 1), (64, 37), (96, 130), (160, 258), (4128, 1001)])
+def test_dequantize_colwise_ragged(fmt, out_dtype, shape):
+    # column-wise codes [cols][rows] of random bytes and random scales: odd
+    # and ragged column counts (scalar tail stores), partial row and column
+    # tiles
+    R, C = shape
+    g = torch.Generator().manual_seed(R * 7 + C)
+    cb = R // 2 if fmt == "e2m1" else R
+    codes = torch.randint(0, 256, (C, cb), dtype=torch.uint8, generator=g)
+    scales = torch.randint(90, 170, (C, R // 32), dtype=torch.uint8, generator=g)
+    got = mxq.mx_dequantize(codes.cuda(), scales.cuda(), R, C, "col", fmt, out_dtype)
+    mxq.check()
+    out = "f32" if out_dtype == torch.float32 else "bf16"
+    exp = O.mx_dequantize(codes.numpy(), scales.numpy(), fmt, out).T
+    np.testing.assert_array_equal(to_np(got.float()), exp)
+
+
 def test_small_round_trip_workload():
     # 256x1024 N(0,1) with 1% x100 outliers, E4M3 row-wise, then dequantize
     x = synth.quantize_dequantize_small()["x"].cuda()
