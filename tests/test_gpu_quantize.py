@@ -82,6 +82,27 @@ def test_dual_parity(fr, hr, fc, hc, shape):
     np.testing.assert_array_equal(to_np(cc), ec)
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("shape", [(288, 1440), (1056, 2088), (4128, 1056)])
+def test_grouped_tile_order(fmt, shape):
+    # one-byte column-wise outputs visit tiles in groups of 8 tile columns;
+    # these shapes have more than one group, a ragged last group and ragged
+    # tile rows and columns
+    x = synth.normal_with_outliers(shape, shape[0] + shape[1]).cuda()
+    _check(x, "col", fmt, False)
+    _check(x, "col", fmt, True)
+    if shape[1] % 32 == 0:
+        cr, sr, cc, sc = mxq.mx_quantize_dual(x, "e4m3", False, "e4m3", fmt == "e5m2")
+        mxq.check()
+        xn = bf16_to_f32_np(x)
+        ec, es = O.quantize_any(xn, "col", "e4m3", fmt == "e5m2")
+        np.testing.assert_array_equal(to_np(sc), es)
+        np.testing.assert_array_equal(to_np(cc), ec)
+        ec, es = O.quantize_any(xn, "row", "e4m3", False)
+        np.testing.assert_array_equal(to_np(sr), es)
+        np.testing.assert_array_equal(to_np(cr), ec)
+
+
 def _special_tensor(rows, cols, seed):
     rng = np.random.default_rng(seed)
     x = (rng.standard_normal((rows, cols)) * np.exp2(rng.integers(-30, 30, (rows, 1)))).astype(np.float32)
