@@ -604,6 +604,9 @@ CASES = {
     # ablation: column-wise random-sign Hadamard E2M1 with stochastic rounding
     "ablate-col-rhe2m1-sr": ("ablate", (16384, 8192, "col", "e2m1", True, 0xA5A5F00F, True)),
     "ablate-row-e4m3-sr": ("ablate", (16384, 8192, "row", "e4m3", False, 0, True)),
+    # dequantizer: 16384 x 8192 codes back to bf16, column-wise (transposing) and row-wise
+    "dequant-col-e4m3-bf16": ("dequant", (16384, 8192, "col", "e4m3", "bf16")),
+    "dequant-row-e4m3-bf16": ("dequant", (16384, 8192, "row", "e4m3", "bf16")),
 }
 
 
@@ -619,6 +622,9 @@ def _case_bytes(what, args):
     if what == "quant1":
         R, C, _, f = args
         return 2 * R * C + R * C * (0.5 if f == "e2m1" else 1.0) + R * C / 32
+    if what == "dequant":
+        R, C, _, f, od = args
+        return R * C * (0.5 if f == "e2m1" else 1.0) + R * C / 32 + R * C * (4 if od == "f32" else 2)
     M, N, K, fmt, od = args
     eb = 1.0 if fmt != "e2m1" else 0.5
     if what == "gemmq":
@@ -897,6 +903,14 @@ def run_case(name, timed=False):
         x = torch.randn(R, Cc, device="cuda", generator=g).to(torch.bfloat16)
         out = mxq.mx_quantize(x, axis, f)
         launch = lambda: mxq.mx_quantize(x, axis, f, out=out)
+    elif what == "dequant":
+        R, Cc, axis, f, od = args
+        x = torch.randn(R, Cc, device="cuda", generator=g).to(torch.bfloat16)
+        codes, sc = mxq.mx_quantize(x, axis, f)
+        dt = torch.float32 if od == "f32" else torch.bfloat16
+        out = torch.empty((R, Cc), dtype=dt, device="cuda")
+        del x
+        launch = lambda: mxq.mx_dequantize(codes, sc, R, Cc, axis, f, dt, out=out)
     else:
         R, Cc, axis, f, had, mask, sr = args
         x = torch.randn(R, Cc, device="cuda", generator=g).to(torch.bfloat16)
