@@ -354,14 +354,7 @@ def gpu_arm(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "e4m3/e2m1 codes, e8m0 scales, fp32 accumulate",
         "data": "synthetic (seeded Student-t / normal / lognormal-scaled; no dataset or weights)",
-        "config": {
-            "workload": WORKLOAD,
-            "tokens": args.tokens,
-            "layers": [f"{L['name']} {L['fin']}->{L['fout']}" for L in plan],
-            "l2": "inputs larger than L2: each step streams ~%.1f GB of distinct tensors" %
-                  ((qbytes) / 1e9),
-            "parallelism": "replicas" if world > 1 else "single GPU",
-        },
+        "config": run_config(plan, args.tokens, world),
         "breakdown": {
             "quantizers": {"GB/s": round(q_gbs, 1), "frac_of_hbm": round(q_gbs / peaks["hbm_gbs"], 3),
                             "ms_per_step": round(sums["q"] / args.steps, 4),
@@ -560,6 +553,19 @@ def cpu_baseline(budget_s=15.0):
                        f"{dt:.1f} s, numpy (BLAS threads = cores)")}
 
 
+def run_config(plan, tokens, world):
+    """The `config` object of both arms' JSON lines (the same workload)."""
+    qbytes = step_work(plan)[0]
+    return {
+        "workload": WORKLOAD,
+        "tokens": tokens,
+        "layers": [f"{L['name']} {L['fin']}->{L['fout']}" for L in plan],
+        "l2": "inputs larger than L2: each step streams ~%.1f GB of distinct tensors" %
+              (qbytes / 1e9),
+        "parallelism": "replicas" if world > 1 else "single GPU",
+    }
+
+
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
@@ -582,7 +588,7 @@ def reference_arm(args, rank, world):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / args.steps, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "tokens": args.tokens},
+        "data": "synthetic", "config": run_config(plan, args.tokens, world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

@@ -57,3 +57,24 @@ def test_step_work_counts():
     macs = sum(L["T"] * L["fin"] * L["fout"] for L in plan)
     assert f8 == 4 * macs and f4 == 2 * macs
     assert bench.quant_bytes(32, 64, "e4m3", "e2m1") == 2 * 2048 + 2048 + 64 + 1024 + 64
+
+
+@pytest.mark.timeout(300)
+def test_reference_arm_line_matches_the_contract():
+    # the oracle arm: rank 0 only, the main arm's metric, unit and config,
+    # and the keys the reference line carries (impl, cpu_baseline, e2e with
+    # no host-device bytes)
+    import argparse
+
+    import bench
+    args = argparse.Namespace(steps=1, warmup=0, tokens=8192)
+    assert bench.reference_arm(args, 1, 2) is None
+    line = bench.reference_arm(args, 0, 1)
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == "TFLOP/s"
+    assert line["higher_is_better"] is True
+    assert line["config"] == bench.run_config(bench.layer_plan(8192), 8192, 1)
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
