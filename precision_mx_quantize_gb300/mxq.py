@@ -194,6 +194,80 @@ def code_shape(rows: int, cols: int, axis, fmt):
     return (r, c // 2 if f == E2M1 else c), (r, c // 32)
 
 
+# The kernels get raw pointers and sizes: a host tensor, or a buffer shorter
+# than the sizes imply, would be read or written past its end on the GPU.
+# These checks run before every launch (explicit raises, not asserts, so
+# that they survive python -O).
+
+def _on_gpu(t):
+    return t.is_cuda
+
+
+def _need(t, name, dtype, numel, device=None):
+    """Raise unless t is a contiguous CUDA tensor of `dtype` (None: any) with
+    at least `numel` elements, on `device` when given."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements; {numel} are needed")
+    if not _on_gpu(t):
+        raise ValueError(f"{name} must be on a CUDA device (the library has no CPU path)")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the inputs on {device}")
+
+
+def _need_input(x):
+    """x: a contiguous 2-D bf16 CUDA tensor."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError("x must be a 2-D torch.Tensor [rows, cols]")
+    _need(x, "x", torch.bfloat16, 0)
+
+
+def _prod(shape):
+    n = 1
+    for d in shape:
+        n *= int(d)
+    return n
+
+
+def _scale_bytes(lines, blocked, scale_layout):
+    """Bytes of the scales of `lines` lines of `blocked` elements in a layout."""
+    if SCALE_LAYOUTS[scale_layout] == SCALES_TC:
+        n = int(mxq_scales_tc_bytes(lines, blocked))
+        if n == 0:
+            raise ValueError(f"no tensor-core scale layout for {lines} lines x {blocked}")
+        return n
+    return lines * (blocked // 32)
+
+
+def _need_codes(codes, scales, rows, cols, axis, fmt, scale_layout, device, tag=""):
+    """The code and scale buffers of a [rows, cols] tensor quantized along `axis`."""
+    cs, _ = code_shape(rows, cols, axis, fmt)
+    lines, blocked = (rows, cols) if AXES[axis] == ROWWISE else (cols, rows)
+    _need(codes, "codes" + tag, torch.uint8, _prod(cs), device)
+    _need(scales, "scales" + tag, torch.uint8, _scale_bytes(lines, blocked, scale_layout), device)
+
+
+def _out_code(out_dtype):
+    if out_dtype == torch.float32:
+        return OUT_F32
+    if out_dtype == torch.bfloat16:
+        return OUT_BF16
+    raise ValueError(f"out_dtype must be torch.float32 or torch.bfloat16, got {out_dtype}")
+
+
+def _need_operands(A, sA, B, sB, fmt, M, N, K, scale_layout):
+    """GEMM operands: K-major codes of A [M, K] and B [N, K] and their scales."""
+    _need(A, "A", torch.uint8, 0)
+    dev = A.device
+    _need_codes(A, sA, M, K, "row", fmt, scale_layout, dev, "_A")
+    _need_codes(B, sB, N, K, "row", fmt, scale_layout, dev, "_B")
+
+
 def _alloc_codes(x, axis, fmt, scale_layout="rowmajor"):
     cs, ss = code_shape(x.shape[0], x.shape[1], axis, fmt)
     if SCALE_LAYOUTS[scale_layout] == SCALES_TC:
@@ -211,8 +285,9 @@ def mx_quantize(x: torch.Tensor, axis="row", fmt="e4m3", out=None, scale_layout=
 
     scale_layout "tc": scales in the tensor cores' chunk layout (a flat byte
     tensor), which mx_gemm(..., scale_layout="tc") reads in place."""
-    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    _need_input(x)
     codes, scales = out if out is not None else _alloc_codes(x, axis, fmt, scale_layout)
+    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, scale_layout, x.device)
     if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
         _ok(mxq_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
                          codes.data_ptr(), scales.data_ptr(), _stream(x.device)), "mxq_quantize")
@@ -226,8 +301,9 @@ def mx_quantize(x: torch.Tensor, axis="row", fmt="e4m3", out=None, scale_layout=
 def hadamard_mx_quantize(x: torch.Tensor, axis="col", fmt="e2m1", out=None,
                          scale_layout="rowmajor"):
     """Fixed 32-point Hadamard rotation of each block, then MX quantization."""
-    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    _need_input(x)
     codes, scales = out if out is not None else _alloc_codes(x, axis, fmt, scale_layout)
+    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, scale_layout, x.device)
     if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
         _ok(mxq_hadamard_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
                                   codes.data_ptr(), scales.data_ptr(), _stream(x.device)),
@@ -242,12 +318,14 @@ def hadamard_mx_quantize(x: torch.Tensor, axis="col", fmt="e2m1", out=None,
 def mx_quantize_dual(x: torch.Tensor, fmt_r="e4m3", had_r=False, fmt_c="e2m1", had_c=True,
                      out=None, scale_layout="rowmajor"):
     """One pass producing the row-wise and the column-wise (transposed) outputs."""
-    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    _need_input(x)
     if out is None:
         cr, sr = _alloc_codes(x, "row", fmt_r, scale_layout)
         cc, sc = _alloc_codes(x, "col", fmt_c, scale_layout)
     else:
         cr, sr, cc, sc = out
+    _need_codes(cr, sr, x.shape[0], x.shape[1], "row", fmt_r, scale_layout, x.device, "_r")
+    _need_codes(cc, sc, x.shape[0], x.shape[1], "col", fmt_c, scale_layout, x.device, "_c")
     if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
         _ok(mxq_quantize_dual(x.data_ptr(), x.shape[0], x.shape[1], FMTS[fmt_r], int(had_r),
                               cr.data_ptr(), sr.data_ptr(), FMTS[fmt_c], int(had_c), cc.data_ptr(),
@@ -265,8 +343,9 @@ def mx_quantize_ablation(x: torch.Tensor, axis="col", fmt="e2m1", hadamard=True,
     """MX quantization with a random-sign Hadamard rotation (sign_mask) and/or
     stochastic rounding (Philox bits keyed by seed); the ablation of the
     deterministic path."""
-    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    _need_input(x)
     codes, scales = out if out is not None else _alloc_codes(x, axis, fmt)
+    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, "rowmajor", x.device)
     _ok(mxq_quantize_ablation(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
                               int(hadamard), int(sign_mask) & 0xFFFFFFFF, int(stochastic),
                               int(seed) & 0xFFFFFFFFFFFFFFFF, codes.data_ptr(), scales.data_ptr(),
@@ -277,9 +356,12 @@ def mx_quantize_ablation(x: torch.Tensor, axis="col", fmt="e2m1", hadamard=True,
 def mx_dequantize(codes, scales, rows, cols, axis="row", fmt="e4m3", out_dtype=torch.float32,
                   out=None):
     """Dequantize codes written by mx_quantize back to a [rows, cols] tensor."""
-    od = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
+    od = _out_code(out_dtype)
+    _need(codes, "codes", torch.uint8, 0)
+    _need_codes(codes, scales, rows, cols, axis, fmt, "rowmajor", codes.device)
     if out is None:
         out = torch.empty((rows, cols), dtype=out_dtype, device=codes.device)
+    _need(out, "out", out_dtype, rows * cols, codes.device)
     _ok(mxq_dequantize(codes.data_ptr(), scales.data_ptr(), rows, cols, AXES[axis], FMTS[fmt],
                        out.data_ptr(), od, _stream(codes.device)), "mxq_dequantize")
     return out
@@ -295,9 +377,11 @@ def mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=torch.float32, out=None, works
     """C[M, N] = dec(A) @ dec(B)^T on the tensor cores (A, B K-major MX codes).
 
     scale_layout "tc": sA, sB in the tensor cores' chunk layout (no workspace)."""
-    od = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
+    od = _out_code(out_dtype)
+    _need_operands(A, sA, B, sB, fmt, M, N, K, scale_layout)
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    _need(out, "out", out_dtype, M * N, A.device)
     if SCALE_LAYOUTS[scale_layout] == SCALES_TC:
         _ok(mxq_gemm_ex(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M, N,
                         K, out.data_ptr(), od, SCALES_TC, None, 0, _stream(A.device)),
@@ -305,6 +389,7 @@ def mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=torch.float32, out=None, works
         return out
     if workspace is None:
         workspace = gemm_workspace(M, N, K, fmt, A.device)
+    _need(workspace, "workspace", torch.uint8, 0, A.device)   # its size is checked by the library
     _ok(mxq_gemm(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M, N, K,
                  out.data_ptr(), od, workspace.data_ptr(), workspace.numel(),
                  _stream(A.device)), "mxq_gemm")
@@ -317,6 +402,7 @@ def mx_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt="e4m3", out=None, works
     fp32 product (blocks of 32 along N); returns (codes, scales)."""
     in_tc = SCALE_LAYOUTS[scale_layout] == SCALES_TC
     out_tc = SCALE_LAYOUTS[out_scale_layout] == SCALES_TC
+    _need_operands(A, sA, B, sB, fmt, M, N, K, scale_layout)
     if out is None:
         cs, ss = code_shape(M, N, "row", out_fmt)
         if out_tc:
@@ -324,6 +410,9 @@ def mx_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt="e4m3", out=None, works
         out = (torch.empty(cs, dtype=torch.uint8, device=A.device),
                torch.empty(ss, dtype=torch.uint8, device=A.device))
     codes, scales = out
+    _need_codes(codes, scales, M, N, "row", out_fmt, out_scale_layout, A.device, "_out")
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 0, A.device)
     if not in_tc and not out_tc:
         if workspace is None:
             workspace = gemm_workspace(M, N, K, fmt, A.device)
