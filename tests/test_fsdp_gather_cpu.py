@@ -52,7 +52,7 @@ def _worker(rank, world, port, fmt, out):
 @pytest.mark.parametrize("world", [2, 4])
 @pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
 def test_gathered_codes_equal_whole_weight_quantization(world, fmt):
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(world, _free_port(), fmt, out), nprocs=world, join=True)
     ec, es = O.mx_quantize(_weight(256, 96).float().numpy(), "row", fmt)
