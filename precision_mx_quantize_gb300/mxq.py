@@ -13,6 +13,7 @@ statement: ``mx_quantize``, ``hadamard_mx_quantize``, ``mx_quantize_dual``,
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -203,21 +204,22 @@ def _on_gpu(t):
     return t.is_cuda
 
 
-def _need(t, name, dtype, numel, device=None):
+def _need(t, name, dtype, numel, dev=None):
     """Raise unless t is a contiguous CUDA tensor of `dtype` (None: any) with
-    at least `numel` elements, on `device` when given."""
+    at least `numel` elements, on device index `dev` when given.  Cheap on
+    the success path (the binding runs it on every call)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
-    if dtype is not None and t.dtype != dtype:
+    if dtype is not None and t.dtype is not dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
     if t.numel() < numel:
         raise ValueError(f"{name} holds {t.numel()} elements; {numel} are needed")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
     if not _on_gpu(t):
         raise ValueError(f"{name} must be on a CUDA device (the library has no CPU path)")
-    if device is not None and t.device != device:
-        raise ValueError(f"{name} is on {t.device}, the inputs on {device}")
+    if dev is not None and t.get_device() != dev:
+        raise ValueError(f"{name} is on device {t.get_device()}, the inputs on {dev}")
 
 
 def _need_input(x):
@@ -227,45 +229,44 @@ def _need_input(x):
     _need(x, "x", torch.bfloat16, 0)
 
 
-def _prod(shape):
-    n = 1
-    for d in shape:
-        n *= int(d)
-    return n
-
-
-def _scale_bytes(lines, blocked, scale_layout):
-    """Bytes of the scales of `lines` lines of `blocked` elements in a layout."""
+@functools.lru_cache(maxsize=4096)
+def _buffer_sizes(rows, cols, axis, fmt, scale_layout):
+    """(code bytes, scale bytes) of a [rows, cols] tensor quantized along
+    `axis`, with its scales in `scale_layout`."""
+    cs, _ = code_shape(rows, cols, axis, fmt)
+    lines, blocked = (rows, cols) if AXES[axis] == ROWWISE else (cols, rows)
     if SCALE_LAYOUTS[scale_layout] == SCALES_TC:
         n = int(mxq_scales_tc_bytes(lines, blocked))
         if n == 0:
             raise ValueError(f"no tensor-core scale layout for {lines} lines x {blocked}")
-        return n
-    return lines * (blocked // 32)
+    else:
+        n = lines * (blocked // 32)
+    return cs[0] * cs[1], n
 
 
-def _need_codes(codes, scales, rows, cols, axis, fmt, scale_layout, device, tag=""):
+def _need_codes(codes, scales, rows, cols, axis, fmt, scale_layout, dev, tag=""):
     """The code and scale buffers of a [rows, cols] tensor quantized along `axis`."""
-    cs, _ = code_shape(rows, cols, axis, fmt)
-    lines, blocked = (rows, cols) if AXES[axis] == ROWWISE else (cols, rows)
-    _need(codes, "codes" + tag, torch.uint8, _prod(cs), device)
-    _need(scales, "scales" + tag, torch.uint8, _scale_bytes(lines, blocked, scale_layout), device)
+    nc, ns = _buffer_sizes(int(rows), int(cols), axis, fmt, scale_layout)
+    _need(codes, "codes" + tag, torch.uint8, nc, dev)
+    _need(scales, "scales" + tag, torch.uint8, ns, dev)
 
 
 def _out_code(out_dtype):
-    if out_dtype == torch.float32:
+    if out_dtype is torch.float32:
         return OUT_F32
-    if out_dtype == torch.bfloat16:
+    if out_dtype is torch.bfloat16:
         return OUT_BF16
     raise ValueError(f"out_dtype must be torch.float32 or torch.bfloat16, got {out_dtype}")
 
 
 def _need_operands(A, sA, B, sB, fmt, M, N, K, scale_layout):
-    """GEMM operands: K-major codes of A [M, K] and B [N, K] and their scales."""
+    """GEMM operands: K-major codes of A [M, K] and B [N, K] and their scales.
+    Returns the device index of A."""
     _need(A, "A", torch.uint8, 0)
-    dev = A.device
+    dev = A.get_device()
     _need_codes(A, sA, M, K, "row", fmt, scale_layout, dev, "_A")
     _need_codes(B, sB, N, K, "row", fmt, scale_layout, dev, "_B")
+    return dev
 
 
 def _alloc_codes(x, axis, fmt, scale_layout="rowmajor"):
@@ -287,7 +288,7 @@ def mx_quantize(x: torch.Tensor, axis="row", fmt="e4m3", out=None, scale_layout=
     tensor), which mx_gemm(..., scale_layout="tc") reads in place."""
     _need_input(x)
     codes, scales = out if out is not None else _alloc_codes(x, axis, fmt, scale_layout)
-    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, scale_layout, x.device)
+    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, scale_layout, x.get_device())
     if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
         _ok(mxq_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
                          codes.data_ptr(), scales.data_ptr(), _stream(x.device)), "mxq_quantize")
@@ -303,7 +304,7 @@ def hadamard_mx_quantize(x: torch.Tensor, axis="col", fmt="e2m1", out=None,
     """Fixed 32-point Hadamard rotation of each block, then MX quantization."""
     _need_input(x)
     codes, scales = out if out is not None else _alloc_codes(x, axis, fmt, scale_layout)
-    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, scale_layout, x.device)
+    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, scale_layout, x.get_device())
     if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
         _ok(mxq_hadamard_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
                                   codes.data_ptr(), scales.data_ptr(), _stream(x.device)),
@@ -324,8 +325,8 @@ def mx_quantize_dual(x: torch.Tensor, fmt_r="e4m3", had_r=False, fmt_c="e2m1", h
         cc, sc = _alloc_codes(x, "col", fmt_c, scale_layout)
     else:
         cr, sr, cc, sc = out
-    _need_codes(cr, sr, x.shape[0], x.shape[1], "row", fmt_r, scale_layout, x.device, "_r")
-    _need_codes(cc, sc, x.shape[0], x.shape[1], "col", fmt_c, scale_layout, x.device, "_c")
+    _need_codes(cr, sr, x.shape[0], x.shape[1], "row", fmt_r, scale_layout, x.get_device(), "_r")
+    _need_codes(cc, sc, x.shape[0], x.shape[1], "col", fmt_c, scale_layout, x.get_device(), "_c")
     if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
         _ok(mxq_quantize_dual(x.data_ptr(), x.shape[0], x.shape[1], FMTS[fmt_r], int(had_r),
                               cr.data_ptr(), sr.data_ptr(), FMTS[fmt_c], int(had_c), cc.data_ptr(),
@@ -345,7 +346,7 @@ def mx_quantize_ablation(x: torch.Tensor, axis="col", fmt="e2m1", hadamard=True,
     deterministic path."""
     _need_input(x)
     codes, scales = out if out is not None else _alloc_codes(x, axis, fmt)
-    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, "rowmajor", x.device)
+    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, "rowmajor", x.get_device())
     _ok(mxq_quantize_ablation(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
                               int(hadamard), int(sign_mask) & 0xFFFFFFFF, int(stochastic),
                               int(seed) & 0xFFFFFFFFFFFFFFFF, codes.data_ptr(), scales.data_ptr(),
@@ -358,10 +359,11 @@ def mx_dequantize(codes, scales, rows, cols, axis="row", fmt="e4m3", out_dtype=t
     """Dequantize codes written by mx_quantize back to a [rows, cols] tensor."""
     od = _out_code(out_dtype)
     _need(codes, "codes", torch.uint8, 0)
-    _need_codes(codes, scales, rows, cols, axis, fmt, "rowmajor", codes.device)
+    dev = codes.get_device()
+    _need_codes(codes, scales, rows, cols, axis, fmt, "rowmajor", dev)
     if out is None:
         out = torch.empty((rows, cols), dtype=out_dtype, device=codes.device)
-    _need(out, "out", out_dtype, rows * cols, codes.device)
+    _need(out, "out", out_dtype, rows * cols, dev)
     _ok(mxq_dequantize(codes.data_ptr(), scales.data_ptr(), rows, cols, AXES[axis], FMTS[fmt],
                        out.data_ptr(), od, _stream(codes.device)), "mxq_dequantize")
     return out
@@ -378,10 +380,10 @@ def mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=torch.float32, out=None, works
 
     scale_layout "tc": sA, sB in the tensor cores' chunk layout (no workspace)."""
     od = _out_code(out_dtype)
-    _need_operands(A, sA, B, sB, fmt, M, N, K, scale_layout)
+    dev = _need_operands(A, sA, B, sB, fmt, M, N, K, scale_layout)
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
-    _need(out, "out", out_dtype, M * N, A.device)
+    _need(out, "out", out_dtype, M * N, dev)
     if SCALE_LAYOUTS[scale_layout] == SCALES_TC:
         _ok(mxq_gemm_ex(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M, N,
                         K, out.data_ptr(), od, SCALES_TC, None, 0, _stream(A.device)),
@@ -389,7 +391,7 @@ def mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=torch.float32, out=None, works
         return out
     if workspace is None:
         workspace = gemm_workspace(M, N, K, fmt, A.device)
-    _need(workspace, "workspace", torch.uint8, 0, A.device)   # its size is checked by the library
+    _need(workspace, "workspace", torch.uint8, 0, dev)   # its size is checked by the library
     _ok(mxq_gemm(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(), FMTS[fmt], M, N, K,
                  out.data_ptr(), od, workspace.data_ptr(), workspace.numel(),
                  _stream(A.device)), "mxq_gemm")
@@ -402,7 +404,7 @@ def mx_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt="e4m3", out=None, works
     fp32 product (blocks of 32 along N); returns (codes, scales)."""
     in_tc = SCALE_LAYOUTS[scale_layout] == SCALES_TC
     out_tc = SCALE_LAYOUTS[out_scale_layout] == SCALES_TC
-    _need_operands(A, sA, B, sB, fmt, M, N, K, scale_layout)
+    dev = _need_operands(A, sA, B, sB, fmt, M, N, K, scale_layout)
     if out is None:
         cs, ss = code_shape(M, N, "row", out_fmt)
         if out_tc:
@@ -410,9 +412,9 @@ def mx_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt="e4m3", out=None, works
         out = (torch.empty(cs, dtype=torch.uint8, device=A.device),
                torch.empty(ss, dtype=torch.uint8, device=A.device))
     codes, scales = out
-    _need_codes(codes, scales, M, N, "row", out_fmt, out_scale_layout, A.device, "_out")
+    _need_codes(codes, scales, M, N, "row", out_fmt, out_scale_layout, dev, "_out")
     if workspace is not None:
-        _need(workspace, "workspace", torch.uint8, 0, A.device)
+        _need(workspace, "workspace", torch.uint8, 0, dev)
     if not in_tc and not out_tc:
         if workspace is None:
             workspace = gemm_workspace(M, N, K, fmt, A.device)
