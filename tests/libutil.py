@@ -44,3 +44,24 @@ def header_symbols():
             src = open(os.path.join(inc, f)).read()
             names |= set(re.findall(r"\b(mxq_[a-z0-9_]+)\s*\(", src))
     return sorted(names)
+
+
+def header_prototypes():
+    """{function name: [parameter declarations]} of the functions the headers
+    declare (comments stripped; a prototype is a name, a parenthesised
+    parameter list and a semicolon)."""
+    import re
+    here = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    inc = os.path.join(here, "include")
+    out = {}
+    for f in os.listdir(inc):
+        if not f.endswith(".h"):
+            continue
+        src = open(os.path.join(inc, f)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        for m in re.finditer(r"\b(mxq_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src):
+            params = m.group(2).strip()
+            out[m.group(1)] = [] if params in ("", "void") else [
+                " ".join(q.split()) for q in params.split(",")]
+    return out

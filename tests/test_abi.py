@@ -6,7 +6,7 @@ import ctypes
 import pytest
 
 from precision_mx_quantize_gb300 import mxq
-from tests.libutil import ensure_built, header_symbols
+from tests.libutil import ensure_built, header_prototypes, header_symbols
 
 
 @pytest.fixture(scope="module")
@@ -71,3 +71,30 @@ def test_tc_scale_buffer_sizes(lib):
     assert mxq.mxq_scales_tc_bytes(8192, 4096) == 64 * 32 * 512 == 8192 * 4096 // 32
     assert mxq.mxq_scales_tc_bytes(64, 96) == 0
     assert mxq.mxq_scales_tc_bytes(0, 128) == 0
+
+
+def _ctype_of(decl):
+    """The ctypes type a C parameter declaration needs (pointers as void*)."""
+    if "*" in decl:
+        return "ptr"
+    t = decl.replace("const ", "").split()[0]
+    return {"int64_t": ctypes.c_int64, "int": ctypes.c_int, "size_t": ctypes.c_size_t,
+            "uint64_t": ctypes.c_uint64, "uint32_t": ctypes.c_uint32}[t]
+
+
+def test_binding_signatures_match_the_header():
+    # a ctypes signature with a missing or mistyped parameter would hand the
+    # library shifted arguments (and the GPU a wrong pointer): every bound
+    # function takes exactly the header's parameters, in order
+    protos = header_prototypes()
+    sigs = {n: args for n, _, args in mxq.SIGNATURES}
+    assert set(protos) == set(sigs)
+    for name, decls in protos.items():
+        args = sigs[name]
+        assert len(args) == len(decls), name
+        for i, (decl, arg) in enumerate(zip(decls, args)):
+            want = _ctype_of(decl)
+            if want == "ptr":
+                assert arg in (ctypes.c_void_p, ctypes.c_char_p), (name, i, decl)
+            else:
+                assert arg is want, (name, i, decl, arg)
