@@ -58,3 +58,27 @@ def load_e2m1_values():
             c, v = line.split()
             vals[int(c)] = float(v)
     return vals
+
+
+def load_e2m1_packed():
+    """List of dicts: name, x (32 floats), scale (int), packed (16 ints) --
+    hand-derived E2M1 blocks with their packed code bytes."""
+    cases, cur = [], None
+    with open(os.path.join(HERE, "e2m1_packed.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rest = line.partition(" ")
+            if key == "case":
+                cur = {"name": rest}
+                cases.append(cur)
+            elif key == "x":
+                cur["x"] = _expand(rest.split(), _num)
+            elif key == "scale":
+                cur["scale"] = int(rest)
+            elif key == "packed":
+                cur["packed"] = _expand(rest.split(), lambda t: int(t, 16))
+    for c in cases:
+        assert len(c["x"]) == 32 and len(c["packed"]) == 16, c["name"]
+    return cases

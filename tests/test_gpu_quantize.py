@@ -12,7 +12,7 @@ import torch
 
 from oracle import mx_oracle as O
 from precision_mx_quantize_gb300 import mxq, synth
-from tests.golden.fixtures import load_blocks
+from tests.golden.fixtures import load_blocks, load_e2m1_packed
 from tests.libutil import bf16_to_f32_np, ensure_built, to_np
 
 pytestmark = pytest.mark.gpu
@@ -137,6 +137,45 @@ def test_hand_derived_blocks_on_gpu(case):
         c = O.unpack_e2m1(c)
     assert int(to_np(scales)[0, 0]) == case["scale"]
     assert [int(v) for v in c] == case["codes"]
+
+
+def test_e2m1_packed_bytes_hand_derived_on_gpu():
+    # the kernels' packed bytes against the hand-derived golden, never
+    # unpacked (element 2j in the low nibble): row-wise one block per row,
+    # column-wise the same blocks down the columns (8 columns, the last ones
+    # zero), and both layouts of the one-pass quantizer
+    cases = load_e2m1_packed()
+    n = len(cases)
+    x = torch.tensor([c["x"] for c in cases], dtype=torch.float32)      # [n, 32]
+    packed = np.array([c["packed"] for c in cases], dtype=np.uint8)
+    scales = np.array([[c["scale"]] for c in cases], dtype=np.uint8)
+    xr = x.to(torch.bfloat16).cuda()
+    codes, sc = mxq.mx_quantize(xr, "row", "e2m1")
+    mxq.check()
+    np.testing.assert_array_equal(to_np(codes), packed)
+    np.testing.assert_array_equal(to_np(sc), scales)
+    xc = torch.zeros((32, 8), dtype=torch.float32)
+    xc[:, :n] = x.T
+    xc = xc.to(torch.bfloat16).cuda()
+    codes, sc = mxq.mx_quantize(xc, "col", "e2m1")
+    mxq.check()
+    np.testing.assert_array_equal(to_np(codes)[:n], packed)
+    np.testing.assert_array_equal(to_np(sc)[:n], scales)
+    assert not to_np(codes)[n:].any() and not to_np(sc)[n:].any()
+    # one-pass quantizer, E2M1 along both axes: the blocks as the first rows
+    # of a 32x32 tile (row-wise output checked), then as its first columns
+    # (column-wise output checked)
+    xd = torch.zeros((32, 32), dtype=torch.float32)
+    xd[:n, :] = x
+    cr, sr, _, _ = mxq.mx_quantize_dual(xd.to(torch.bfloat16).cuda(), "e2m1", False, "e2m1", False)
+    mxq.check()
+    np.testing.assert_array_equal(to_np(cr)[:n], packed)
+    np.testing.assert_array_equal(to_np(sr)[:n], scales)
+    _, _, cc, scc = mxq.mx_quantize_dual(xd.T.contiguous().to(torch.bfloat16).cuda(), "e2m1", False,
+                                         "e2m1", False)
+    mxq.check()
+    np.testing.assert_array_equal(to_np(cc)[:n], packed)
+    np.testing.assert_array_equal(to_np(scc)[:n], scales)
 
 
 @pytest.mark.parametrize("fmt", FMTS)

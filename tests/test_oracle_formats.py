@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from oracle import mx_oracle as O
-from tests.golden.fixtures import load_blocks, load_e2m1_values
+from tests.golden.fixtures import load_blocks, load_e2m1_packed, load_e2m1_values
 
 
 def test_e4m3_decode_matches_torch_float8():
@@ -126,6 +126,34 @@ def test_hand_derived_blocks(case):
         codes = O.unpack_e2m1(codes)
     assert int(s[0, 0]) == case["scale"]
     assert [int(c) for c in codes[0]] == case["codes"]
+
+
+def test_e2m1_packed_bytes_hand_derived():
+    # the packed bytes themselves, never unpacked: element 2j in the low
+    # nibble (reading R5), on hand-derived blocks whose 16 bytes all differ
+    # from their own nibble swap; row-wise one block per row, column-wise the
+    # same blocks down the columns, stored transposed (R6)
+    cases = load_e2m1_packed()
+    x = np.array([c["x"] for c in cases], dtype=np.float32)            # [n, 32]
+    xb = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(xb, x)                                        # exact bf16 inputs
+    packed = np.array([c["packed"] for c in cases], dtype=np.uint8)     # [n, 16]
+    scales = np.array([[c["scale"]] for c in cases], dtype=np.uint8)
+    codes, s = O.mx_quantize(x, "row", O.E2M1)
+    assert codes.dtype == np.uint8 and codes.shape == (len(cases), 16)
+    np.testing.assert_array_equal(codes, packed)
+    np.testing.assert_array_equal(s, scales)
+    codes_c, s_c = O.mx_quantize(np.ascontiguousarray(x.T), "col", O.E2M1)
+    np.testing.assert_array_equal(codes_c, packed)
+    np.testing.assert_array_equal(s_c, scales)
+
+
+def test_e2m1_golden_bytes_are_not_nibble_symmetric():
+    # a nibble-swapped packing would fail the test above on every byte of
+    # the first two blocks
+    for c in load_e2m1_packed()[:2]:
+        for b in c["packed"]:
+            assert (b & 0xF) != (b >> 4)
 
 
 def _representable_block(rng, fmt, R, C):
