@@ -328,6 +328,14 @@ def gpu_arm(args, rank, world, local_rank):
     # ---- end to end through the public API with host buffers
     e2e = e2e_measure(args, layers, flops, device)
 
+    # ---- the other configurations, each timed on its own (after the timed
+    # region, so they do not touch the headline number)
+    configs = None
+    if not args.no_configs and world == 1:
+        del layers
+        torch.cuda.empty_cache()
+        configs = config_cases(_peaks())
+
     ms_max = reduce_max_ms(ms_total, device)
     if rank != 0:
         return None
@@ -338,8 +346,9 @@ def gpu_arm(args, rank, world, local_rank):
     q_gbs = qbytes * args.steps / (sums["q"] * 1e-3) / 1e9
     f8_tf = f8 * args.steps / (sums["f8"] * 1e-3) / 1e12
     f4_tf = f4 * args.steps / (sums["f4"] * 1e-3) / 1e12
-    fp8_peak = 2.0 * peaks["bf16_sustained"]   # nominal fp8:bf16 = 4.5 : 2.25
-    fp4_peak = 6.0 * peaks["bf16_sustained"]   # nominal fp4:bf16 = 13.5 : 2.25
+    basis, bf16_peak = peak_basis(clocks, peaks)
+    fp8_peak = 2.0 * bf16_peak   # nominal fp8:bf16 = 4.5 : 2.25
+    fp4_peak = 6.0 * bf16_peak   # nominal fp4:bf16 = 13.5 : 2.25
     traffic = _profile_traffic()
     line = {
         "metric": METRIC,
@@ -365,7 +374,8 @@ def gpu_arm(args, rank, world, local_rank):
                            "ms_per_step": round(sums["f4"] / args.steps, 4), "flop_per_step": f4},
             "peaks": {"hbm_GB/s": peaks["hbm_gbs"], "mxfp8_TFLOP/s": fp8_peak,
                       "mxfp4_TFLOP/s": fp4_peak,
-                      "basis": f"{peaks['source']} (MEASURED_PEAKS.json): HBM copy; bf16 sustained x nominal ratio"},
+                      "basis": f"{peaks['source']} (MEASURED_PEAKS.json): HBM copy; bf16 {basis} "
+                               f"x nominal ratio (2x MXFP8, 6x MXFP4)"},
         },
         "roofline": {
             "kernel": "mx_gemm_kernel (MXFP8 E4M3, forward + dgrad launches)",
@@ -374,17 +384,40 @@ def gpu_arm(args, rank, world, local_rank):
             "peak": fp8_peak,
             "unit": "TFLOP/s",
             "frac": round(f8_tf / fp8_peak, 3),
+            "peak_basis": basis,
             "traffic": traffic,
+            "mxfp4": {"kernel": "mx_gemm_kernel (MXFP4 E2M1, Wgrad launches)", "bound": "tensor",
+                      "achieved": round(f4_tf, 1), "peak": fp4_peak, "unit": "TFLOP/s",
+                      "frac": round(f4_tf / fp4_peak, 3)},
+            "quantizers": {"kernel": "mx_quant_kernel (dual passes)", "bound": "hbm",
+                           "achieved": round(q_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": round(q_gbs / peaks["hbm_gbs"], 3)},
             "timing": "CUDA events at the phase boundaries of a second pass of the K timed "
                       "steps; the headline pass has events only around the K steps",
         },
         "e2e": e2e,
+        "configs": configs,
         "gpu_launches": LAUNCHES_PER_LAYER * len(plan) * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
     return line
+
+
+def peak_basis(clocks, peaks):
+    """Which measured bf16 GEMM peak the tensor fractions are taken against.
+
+    The burst figure (a GEMM timed alone, at full clock) applies when the
+    run's own clock samples show the SM clock at its maximum and no power
+    cap; otherwise the sustained figure (a seconds-long GEMM loop under the
+    power cap) does.  Returns (name, bf16 TFLOP/s).
+    """
+    sm, smax = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    capped = "sw_power_cap" in clocks.get("reasons", [])
+    if sm and smax and not capped and sm >= 0.97 * smax:
+        return "burst", peaks["bf16"]
+    return "sustained", peaks["bf16_sustained"]
 
 
 def _profile_traffic():
@@ -540,17 +573,163 @@ def _oracle_sample_step(plan, t_s, out_s, seed=0):
     return flops
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
+def _oracle_dual_band(args):
+    """Dual quantization of one row band in the oracle (a worker of the all-core leg)."""
+    x, fr, hr, fc, hc = args
+    from oracle import mx_oracle as O
+    O.quantize_any(x, "row", fr, hr)
+    O.quantize_any(x, "col", fc, hc)
+    return x.shape[0]
+
+
+def _oracle_quantizer_rates(rows_single=1024):
+    """The oracle's dual Hadamard-E2M1 quantizer (the 8192x4096 activation
+    workload) in GB/s of algorithmic bytes: on one process over a band of
+    `rows_single` rows, and on every core (a spawn pool, one row band per
+    process) over the whole tensor."""
+    import multiprocessing
+
+    from oracle import mx_oracle as O
+    from precision_mx_quantize_gb300 import synth
+    x = synth.hadamard_dual_activation()["x"].float().numpy()
+    R, C = x.shape
+    band = x[:rows_single]
+    t0 = time.perf_counter()
+    O.quantize_any(band, "row", "e2m1", True)
+    O.quantize_any(band, "col", "e2m1", True)
+    dt1 = time.perf_counter() - t0
+    gbs1 = quant_bytes(rows_single, C, "e2m1", "e2m1") / dt1 / 1e9
+    cores = os.cpu_count() or 1
+    step = max(32, (R // cores) // 32 * 32)
+    bands = [(x[r:r + step], "e2m1", True, "e2m1", True) for r in range(0, R, step)]
+    with multiprocessing.get_context("spawn").Pool(cores) as pool:
+        pool.map(_oracle_dual_band, [(x[:32], "e2m1", True, "e2m1", True)] * cores)  # warm
+        t0 = time.perf_counter()
+        pool.map(_oracle_dual_band, bands)
+        dtn = time.perf_counter() - t0
+    gbsn = quant_bytes(R, C, "e2m1", "e2m1") / dtn / 1e9
+    return {"workload": f"dual Hadamard + E2M1 (rows and columns), {R}x{C} activation",
+            "GB/s_one_process": round(gbs1, 4), "sample_one_process": f"{rows_single}x{C} rows band, {dt1:.2f} s",
+            "GB/s_all_cores": round(gbsn, 4), "processes": cores,
+            "sample_all_cores": f"the whole {R}x{C} tensor in {len(bands)} row bands, {dtn:.2f} s"}
+
+
+def _oracle_gemm_rates(M=8192, N=14336, K=4096, rows=512, sample=256, fmt="e4m3"):
+    """The oracle's fp64 GEMM on an M x N x K shape (default: the MLP
+    up-projection, MXFP8): the sampled-element check as MAC/s, and a full
+    product over a `rows`-row slice, extrapolated linearly to all M rows."""
+    import numpy as np
+
+    from oracle import mx_oracle as O
+    rng = np.random.default_rng(0)
+    kb = K if fmt == "e4m3" else K // 2
+    hi = 0x7E if fmt == "e4m3" else 256
+    A = rng.integers(0, hi, size=(rows, kb), dtype=np.uint8)
+    sA = rng.integers(120, 134, size=(rows, K // 32), dtype=np.uint8)
+    B = rng.integers(0, hi, size=(N, kb), dtype=np.uint8)
+    sB = rng.integers(120, 134, size=(N, K // 32), dtype=np.uint8)
+    ri = rng.integers(0, rows, sample)
+    ci = rng.integers(0, N, sample)
+    t0 = time.perf_counter()
+    O.mx_gemm_f64_rows(A, sA, B, sB, fmt, ri, ci)
+    dts = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    O.mx_gemm_f64(A, sA, B, sB, fmt)
+    dtf = time.perf_counter() - t0
+    macs = rows * N * K
+    return {"workload": f"{'MXFP8' if fmt == 'e4m3' else 'MXFP4'} GEMM {M}x{N}x{K} "
+                        "(fp64 over dequantized operands, C and sum|ab|)",
+            "sampled_check_MAC/s": round(sample * sample * K / dts, 1),
+            "sampled_check": f"{sample} rows x {sample} columns, {dts:.2f} s",
+            "slice_MAC/s": round(macs / dtf, 1),
+            "slice": f"{rows} rows x {N} x {K}, {dtf:.2f} s",
+            "full_ms_extrapolated": round(dtf * (M / rows) * 1e3, 1),
+            "extrapolated": True}
+
+
+def _oracle_round_trip_us(reps=5):
+    """The oracle's 256x1024 E4M3 quantize and dequantize, microseconds per call."""
+    from oracle import mx_oracle as O
+    from precision_mx_quantize_gb300 import synth
+    x = synth.quantize_dequantize_small()["x"].float().numpy()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        c, s = O.mx_quantize(x, "row", "e4m3")
+    tq = (time.perf_counter() - t0) / reps
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        O.mx_dequantize(c, s, "e4m3")
+    td = (time.perf_counter() - t0) / reps
+    return {"quantize_us": round(tq * 1e6, 1), "dequantize_us": round(td * 1e6, 1),
+            "sample": f"the whole 256x1024 tensor, mean of {reps} calls, one process"}
+
+
+def _oracle_dequant_rate(fmt, axis, out, rows=512, cols=4096):
+    """The oracle's dequantizer GB/s (algorithmic bytes) on a rows x cols sample."""
+    from oracle import mx_oracle as O
+    from precision_mx_quantize_gb300 import synth
+    x = synth.normal((rows, cols), 0).float().numpy()
+    c, s = O.mx_quantize(x, axis, fmt)
+    t0 = time.perf_counter()
+    O.mx_dequantize(c, s, fmt, out)
+    dt = time.perf_counter() - t0
+    n = rows * cols
+    b = n * ((1 if fmt == "e4m3" else 0.5) + 1 / 32 + (4 if out == "f32" else 2))
+    return {"GB/s": round(b / dt / 1e9, 5), "sample": f"{rows}x{cols}, one process, {dt:.3f} s"}
+
+
+def _oracle_sweep_rate(fmt, layout, had, rows=256, cols=4096):
+    """The oracle's GB/s (algorithmic bytes) for one quantizer-sweep variant on
+    a rows x cols N(0,1) sample, one process."""
+    from oracle import mx_oracle as O
+    from precision_mx_quantize_gb300 import synth
+    x = synth.normal((rows, cols), 0).float().numpy()
+    t0 = time.perf_counter()
+    if layout in ("row", "dual"):
+        O.quantize_any(x, "row", fmt, had)
+    if layout in ("col", "dual"):
+        O.quantize_any(x, "col", fmt, had)
+    dt = time.perf_counter() - t0
+    n = rows * cols
+    one = (n if fmt == "e4m3" else n // 2) + n // 32
+    b = 2 * n + (2 * one if layout == "dual" else one)
+    return {"GB/s": round(b / dt / 1e9, 5), "sample": f"{rows}x{cols}, one process, {dt:.2f} s"}
+
+
 def cpu_baseline(budget_s=15.0):
     t_s, out_s = 512, 2048
     plan = layer_plan(8192)
     t0 = time.perf_counter()
     flops = _oracle_sample_step(plan, t_s, out_s)
     dt = time.perf_counter() - t0
-    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "kind": "oracle",
+    line = {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle", "cpu_model": cpu_model(),
             "sample": (f"every layer of the block pass on {t_s} tokens x {out_s} output features "
                        f"(full input width): 6 quantizations + 3 fp64 GEMMs per layer; "
                        f"{dt:.1f} s, numpy (BLAS threads = cores)")}
+    line["quantizer"] = _oracle_quantizer_rates()
+    line["gemm"] = _oracle_gemm_rates()
+    return line
 
 
 def run_config(plan, tokens, world):
@@ -728,6 +907,94 @@ def _time_rotating(launches, reps=20, warm=5, graph=False):
     return e0.elapsed_time(e1) / reps
 
 
+def config_cases(peaks):
+    """The four configurations besides the block pass, timed on the GPU.
+
+    * cfg1 round trip: 256x1024 N(0,1) with 1% x100 outliers, row-wise E4M3
+      quantize then dequantize to fp32 (latency-bound: microseconds per call,
+      launched one by one from Python, and the kernel time in a CUDA graph);
+    * cfg2: dual Hadamard E2M1 of the 8192x4096 activation (GB/s);
+    * cfg3: MLP up-projection forward GEMM 8192x14336x4096 MXFP8, fp32 out;
+    * cfg4: MLP Wgrad GEMM 14336x4096x16384 MXFP4 on Hadamard E2M1 operands,
+      fp32 out, with its two quantizers (GB/s).
+    Buffers rotate so that each launch reads from HBM.  A GEMM timed alone is
+    set against the burst bf16 figure times the nominal ratio.
+    """
+    import torch
+
+    from precision_mx_quantize_gb300 import mxq, synth
+    hbm = peaks["hbm_gbs"]
+    out = {}
+
+    x = synth.quantize_dequantize_small()["x"].cuda()
+    c, sc = mxq.mx_quantize(x, "row", "e4m3")
+    y = torch.empty((256, 1024), dtype=torch.float32, device="cuda")
+    q1 = lambda: mxq.mx_quantize(x, "row", "e4m3", out=(c, sc))
+    d1 = lambda: mxq.mx_dequantize(c, sc, 256, 1024, "row", "e4m3", out=y)
+    out["cfg1_round_trip_256x1024_e4m3"] = {
+        "config": "round trip 256x1024 E4M3",
+        "quantize_us": round(_time_rotating([q1], reps=200) * 1e3, 2),
+        "dequantize_us": round(_time_rotating([d1], reps=200) * 1e3, 2),
+        "quantize_us_graph": round(_time_rotating([q1], reps=200, graph=True) * 1e3, 2),
+        "dequantize_us_graph": round(_time_rotating([d1], reps=200, graph=True) * 1e3, 2),
+        "timing": "us per call launched one by one from Python; _graph: the same calls in a CUDA graph"}
+    del x, c, sc, y
+
+    x = synth.hadamard_dual_activation()["x"].cuda()
+    xs = [x] + [x.clone() for _ in range(3)]
+    outs = [mxq.mx_quantize_dual(xx, "e2m1", True, "e2m1", True) for xx in xs]
+    ls = [lambda i=i: mxq.mx_quantize_dual(xs[i], "e2m1", True, "e2m1", True, out=outs[i])
+          for i in range(4)]
+    b = quant_bytes(8192, 4096, "e2m1", "e2m1")
+    ms = _time_rotating(ls)
+    msg = _time_rotating(ls, graph=True)
+    out["cfg2_dual_hadamard_e2m1_8192x4096"] = {
+        "config": "dual Hadamard E2M1 8192x4096", "ms": round(ms, 4),
+        "GB/s": round(b / ms / 1e6, 1), "frac_of_hbm": round(b / ms / 1e6 / hbm, 3),
+        "ms_graph": round(msg, 4), "GB/s_graph": round(b / msg / 1e6, 1),
+        "frac_of_hbm_graph": round(b / msg / 1e6 / hbm, 3),
+        "bytes": b}
+    del x, xs, outs, ls
+
+    d = synth.mlp_up_forward()
+    x, w = d["x"].cuda(), d["w"].cuda()
+    A, sA = mxq.mx_quantize(x, "row", "e4m3", scale_layout="tc")
+    B, sB = mxq.mx_quantize(w, "col", "e4m3", scale_layout="tc")
+    C = torch.empty((8192, 14336), dtype=torch.float32, device="cuda")
+    ms = _time_rotating([lambda: mxq.mx_gemm(A, sA, B, sB, "e4m3", 8192, 14336, 4096, out=C,
+                                              scale_layout="tc")])
+    f = 2 * 8192 * 14336 * 4096
+    out["cfg3_mlp_up_fwd_mxfp8_8192x14336x4096"] = {
+        "config": "MLP up forward 8192x14336x4096 MXFP8, fp32 out", "ms": round(ms, 4),
+        "TFLOP/s": round(f / ms / 1e9, 1),
+        "frac_of_peak": round(f / ms / 1e9 / (2 * peaks["bf16"]), 3), "peak_basis": "burst"}
+    del d, x, w, A, B, C
+
+    d = synth.mlp_wgrad()
+    dy, x = d["dy"].cuda(), d["x"].cuda()
+    A, sA = mxq.hadamard_mx_quantize(dy, "col", "e2m1", scale_layout="tc")
+    B, sB = mxq.hadamard_mx_quantize(x, "col", "e2m1", scale_layout="tc")
+    ms_q = _time_rotating([lambda: mxq.hadamard_mx_quantize(dy, "col", "e2m1", out=(A, sA),
+                                                            scale_layout="tc"),
+                           lambda: mxq.hadamard_mx_quantize(x, "col", "e2m1", out=(B, sB),
+                                                            scale_layout="tc")])
+    C = torch.empty((14336, 4096), dtype=torch.float32, device="cuda")
+    ms = _time_rotating([lambda: mxq.mx_gemm(A, sA, B, sB, "e2m1", 14336, 4096, 16384, out=C,
+                                              scale_layout="tc")])
+    f = 2 * 14336 * 4096 * 16384
+    qb = (16384 * 14336 + 16384 * 4096) * (2 + 0.5 + 1 / 32)
+    out["cfg4_mlp_wgrad_mxfp4_14336x4096x16384"] = {
+        "config": "MLP Wgrad 14336x4096x16384 MXFP4 (Hadamard E2M1), fp32 out", "ms": round(ms, 4),
+        "TFLOP/s": round(f / ms / 1e9, 1),
+        "frac_of_peak": round(f / ms / 1e9 / (6 * peaks["bf16"]), 3), "peak_basis": "burst",
+        "quantizers_GB/s": round(qb / (2 * ms_q) / 1e6, 1),
+        "quantizers_frac_of_hbm": round(qb / (2 * ms_q) / 1e6 / hbm, 3)}
+    del d, dy, x, A, B, C
+    mxq.check()
+    torch.cuda.empty_cache()
+    return out
+
+
 def sweep():
     """The measurement configurations besides the block pass, one JSON line each.
 
@@ -753,58 +1020,15 @@ def sweep():
         print(json.dumps(d), flush=True)
         lines.append(d)
 
-    # round trip (latency-bound)
-    x = synth.quantize_dequantize_small()["x"].cuda()
-    c, sc = mxq.mx_quantize(x, "row", "e4m3")
-    out = torch.empty((256, 1024), dtype=torch.float32, device="cuda")
-    ms_q = _time_rotating([lambda: mxq.mx_quantize(x, "row", "e4m3", out=(c, sc))], reps=200)
-    ms_d = _time_rotating([lambda: mxq.mx_dequantize(c, sc, 256, 1024, "row", "e4m3", out=out)], reps=200)
-    emit({"config": "round trip 256x1024 E4M3", "quantize_us": round(ms_q * 1e3, 2),
-          "dequantize_us": round(ms_d * 1e3, 2)})
-
-    # dual Hadamard E2M1 on the 8192x4096 activation
-    x = synth.hadamard_dual_activation()["x"].cuda()
-    outs = [mxq.mx_quantize_dual(x, "e2m1", True, "e2m1", True) for _ in range(4)]
-    xs = [x] + [x.clone() for _ in range(3)]
-    ms = _time_rotating([lambda i=i: mxq.mx_quantize_dual(xs[i], "e2m1", True, "e2m1", True, out=outs[i])
-                         for i in range(4)])
-    b = quant_bytes(8192, 4096, "e2m1", "e2m1")
-    emit({"config": "dual Hadamard E2M1 8192x4096", "ms": round(ms, 4),
-          "GB/s": round(b / ms / 1e6, 1), "frac_of_hbm": round(b / ms / 1e6 / hbm, 3)})
-    del x, xs, outs
-
-    # MLP up-projection forward (MXFP8) and MLP Wgrad (MXFP4)
-    d = synth.mlp_up_forward()
-    x, w = d["x"].cuda(), d["w"].cuda()
-    A, sA = mxq.mx_quantize(x, "row", "e4m3", scale_layout="tc")
-    B, sB = mxq.mx_quantize(w, "col", "e4m3", scale_layout="tc")
-    C = torch.empty((8192, 14336), dtype=torch.float32, device="cuda")
-    ms = _time_rotating([lambda: mxq.mx_gemm(A, sA, B, sB, "e4m3", 8192, 14336, 4096, out=C,
-                                              scale_layout="tc")])
-    f = 2 * 8192 * 14336 * 4096
-    emit({"config": "MLP up forward 8192x14336x4096 MXFP8, fp32 out", "ms": round(ms, 4),
-          "TFLOP/s": round(f / ms / 1e9, 1),
-          "frac_of_peak": round(f / ms / 1e9 / (2 * peaks["bf16_sustained"]), 3)})
-    del d, x, w, A, B, C
-    d = synth.mlp_wgrad()
-    dy, x = d["dy"].cuda(), d["x"].cuda()
-    qa = lambda: mxq.hadamard_mx_quantize(dy, "col", "e2m1", scale_layout="tc")
-    A, sA = qa()
-    B, sB = mxq.hadamard_mx_quantize(x, "col", "e2m1", scale_layout="tc")
-    ms_q = _time_rotating([lambda: mxq.hadamard_mx_quantize(dy, "col", "e2m1", out=(A, sA),
-                                                            scale_layout="tc"),
-                           lambda: mxq.hadamard_mx_quantize(x, "col", "e2m1", out=(B, sB),
-                                                            scale_layout="tc")])
-    C = torch.empty((14336, 4096), dtype=torch.float32, device="cuda")
-    ms = _time_rotating([lambda: mxq.mx_gemm(A, sA, B, sB, "e2m1", 14336, 4096, 16384, out=C,
-                                              scale_layout="tc")])
-    f = 2 * 14336 * 4096 * 16384
-    qb = (16384 * 14336 + 16384 * 4096) * (2 + 0.5 + 1 / 32)
-    emit({"config": "MLP Wgrad 14336x4096x16384 MXFP4 (Hadamard E2M1), fp32 out", "ms": round(ms, 4),
-          "TFLOP/s": round(f / ms / 1e9, 1),
-          "frac_of_peak": round(f / ms / 1e9 / (6 * peaks["bf16_sustained"]), 3),
-          "quantizers_GB/s": round(qb / (2 * ms_q) / 1e6, 1)})
-    del d, dy, x, A, B, C
+    host = {"cores": os.cpu_count(), "cpu_model": cpu_model(), "kind": "oracle"}
+    orates = {"cfg1_round_trip_256x1024_e4m3": _oracle_round_trip_us(),
+              "cfg2_dual_hadamard_e2m1_8192x4096": _oracle_quantizer_rates(),
+              "cfg3_mlp_up_fwd_mxfp8_8192x14336x4096": _oracle_gemm_rates(),
+              "cfg4_mlp_wgrad_mxfp4_14336x4096x16384": _oracle_gemm_rates(
+                  M=14336, N=4096, K=16384, fmt="e2m1")}
+    for k, d in config_cases(peaks).items():
+        d["cpu_oracle"] = dict(host, **orates[k])
+        emit(d)
     torch.cuda.empty_cache()
 
     # dequantizer bandwidth (16384 x 8192 codes -> fp32 / bf16)
@@ -820,7 +1044,9 @@ def sweep():
                 b = n * ((1 if fmt == "e4m3" else 0.5) + 1 / 32 + ob)
                 emit({"config": "dequantize 16384x8192", "fmt": fmt, "layout": axis,
                       "out": str(od).replace("torch.", ""), "us": round(ms * 1e3, 2),
-                      "GB/s": round(b / ms / 1e6, 1), "frac_of_hbm": round(b / ms / 1e6 / hbm, 3)})
+                      "GB/s": round(b / ms / 1e6, 1), "frac_of_hbm": round(b / ms / 1e6 / hbm, 3),
+                      "cpu_oracle": dict(host, **_oracle_dequant_rate(
+                          fmt, axis, "f32" if ob == 4 else "bf16"))})
             del x, c, sc, out
     torch.cuda.empty_cache()
 
@@ -833,6 +1059,7 @@ def sweep():
     for fmt in ("e4m3", "e2m1"):
         for layout in ("row", "col", "dual"):
             for had in (False, True):
+                oracle_rate = dict(host, **_oracle_sweep_rate(fmt, layout, had))
                 for e in range(20, 29):
                     n = 1 << e
                     rows = n // 4096
@@ -857,7 +1084,8 @@ def sweep():
                           "hadamard": had, "elements": n, "us": round(ms * 1e3, 2),
                           "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 3),
                           "us_eager": round(ms_eager * 1e3, 2),
-                          "timing": "CUDA graph of the launches (us_eager: launched one by one)"})
+                          "timing": "CUDA graph of the launches (us_eager: launched one by one)",
+                          "cpu_oracle": oracle_rate})
                     del xs, outs, ls
                     torch.cuda.empty_cache()
     mxq.check()
@@ -975,6 +1203,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the four single-kernel configurations after the block pass")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--case", choices=sorted(CASES) + ["ablate-error"],
                     help="run one kernel case (for ncu) and exit; ablate-error prints the "

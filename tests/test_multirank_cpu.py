@@ -78,3 +78,18 @@ def test_reference_arm_line_matches_the_contract():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_peak_basis_follows_the_clock_samples():
+    # burst bf16 figure when the run held its maximum clock with no power
+    # cap; the sustained figure otherwise
+    import bench
+    peaks = {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6700.0}
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert bench.peak_basis(full, peaks) == ("burst", 1900.0)
+    capped = dict(full, reasons=["sw_power_cap"])
+    assert bench.peak_basis(capped, peaks) == ("sustained", 1700.0)
+    slow = dict(full, sm_mhz=1700.0)
+    assert bench.peak_basis(slow, peaks) == ("sustained", 1700.0)
+    none = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    assert bench.peak_basis(none, peaks) == ("sustained", 1700.0)
