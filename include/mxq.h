@@ -285,6 +285,9 @@ size_t mxq_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int fmt);
  * (with the device current); make that first call before any stream capture.
  * All calls share the buffer: calls that overlap on the GPU (other streams,
  * other host threads) race on it and must be serialized by the caller.
+ * The looked-up address is kept for the life of the process: after
+ * cudaDeviceReset() (or any teardown of the device's primary context) the
+ * entry point must not be called again in that process.
  */
 mxq_status mxq_gemm_noalloc(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
                             int fmt, int64_t M, int64_t N, int64_t K, void* C, int out_dtype,

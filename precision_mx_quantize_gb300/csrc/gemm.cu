@@ -60,6 +60,7 @@ constexpr int G_SFA_BYTES = 1024;            // own 128 rows: up to 2 chunks of 
 constexpr int G_SFB_BYTES = 2048;            // all 256 rows: up to 4 chunks of 512 B
 constexpr int G_STAGE_BYTES = G_A_BYTES + G_B_BYTES + G_SFA_BYTES + G_SFB_BYTES;
 constexpr int G_BAR_BYTES = 512;
+constexpr uint32_t kNotYet = 0xFFFFFFFFu;   // peer's stage count not yet reported
 constexpr int G_SMEM = G_STAGES * G_STAGE_BYTES + G_BAR_BYTES + 1024;
 constexpr uint32_t G_TMEM_COLS = 512;
 constexpr uint32_t G_SFA_COL0 = 256;                 // 8 columns per stage
@@ -221,6 +222,11 @@ MXQ_DEV void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Store a word into shared memory of a CTA of the cluster (`addr` from mapa).
+MXQ_DEV void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 MXQ_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -374,6 +380,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   uint64_t* drain = tmem_empty + 1;
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_slot + 1);
+  // leader: the number of K stages the peer CTA's producer issued, written
+  // by the peer when its producer stops (kNotYet until then)
+  volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(abort_flag + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -392,6 +401,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     mbar_init(smem_u32(tmem_empty), 8 * G_CLUSTER);
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
+    *peer_issued = kNotYet;
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_base_slot), G_TMEM_COLS);
@@ -445,10 +455,28 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           if (++s == G_STAGES) { s = 0; phase ^= 1; }
         }
       }
-      if (!ok && leader) {
-        // bounded wait for the copies of the stages issued last
-        for (uint32_t k = issued > G_STAGES ? issued - G_STAGES : 0; k < issued; ++k)
-          mbar_wait(smem_u32(&full[k % G_STAGES]), (k / G_STAGES) & 1, tmo);
+      if (!leader) {
+        // tell the leader how many stages this CTA's copies were issued for
+        st_cluster_u32(map_to_rank(smem_u32(const_cast<uint32_t*>(peer_issued)), 0), issued);
+      } else if (!ok) {
+        // Every copy of both CTAs signals the leader's stage barriers, and
+        // the peer's land in the peer's shared memory, which stays in use
+        // until the final cluster barrier.  So before that barrier the leader
+        // waits (bounded) for the copies of the last stages either CTA
+        // issued; stages only the peer issued get their expected bytes here.
+        const uint64_t t0 = global_ns();
+        while (*peer_issued == kNotYet && global_ns() - t0 <= 2 * tmo + 1000000) {
+        }
+        uint32_t last = issued;
+        if (*peer_issued != kNotYet && *peer_issued > last) last = *peer_issued;
+        for (uint32_t k = last > G_STAGES ? last - G_STAGES : 0; k < last; ++k) {
+          if (k >= issued) mbar_arrive_expect_tx(smem_u32(&full[k % G_STAGES]), cta_tx);
+          if (!mbar_wait(smem_u32(&full[k % G_STAGES]), (k / G_STAGES) & 1, tmo)) {
+            // a stage one CTA never issued: later stages were not issued either
+            record_error(&g_err_gemm, MXQ_ERR_TIMEOUT, SITE_GEMM_FULL);
+            break;
+          }
+        }
       }
     }
   } else if (warp == 1) {
