@@ -130,6 +130,9 @@ __global__ void __launch_bounds__(256) mx_dequant_rows(const uint8_t* __restrict
   for (IDX i = IDX(blockIdx.x) * blockDim.x + threadIdx.x; i < nv; i += IDX(gridDim.x) * blockDim.x) {
     const IDX e0 = i * V;
     const IDX r = e0 / C, c = e0 - r * C;
+    if (!MXQ_IN_BOUNDS(int64_t(e0) + V <= R64 * C64 && int64_t(c) + V <= C64 && int64_t(r) < R64,
+                       &g_err_quant, SITE_B_DQ_ROWS))
+      continue;
     const float sc = scale_value(scales[int64_t(r) * nsb + (c >> 5)]);
     float f[16];
     if constexpr (BF16) {
@@ -195,6 +198,9 @@ __global__ void __launch_bounds__(256) mx_dequant_cols(const uint8_t* __restrict
     const int cc = blk % TC, b = blk / TC;
     const int64_t c = c0 + cc, rr = r0 + 32 * b;
     if (c >= C || rr >= R) continue;
+    if (!MXQ_IN_BOUNDS(rr + 32 <= R && cc < TC && 32 * b + 32 <= TR, &g_err_quant,
+                       SITE_B_DQ_COLS))
+      continue;
     const float sc = scale_value(scales[c * (R >> 5) + (rr >> 5)]);
     const uint8_t* src = codes + c * col_bytes;
     float f[16], g[16];
@@ -222,6 +228,9 @@ __global__ void __launch_bounds__(256) mx_dequant_cols(const uint8_t* __restrict
     if (r >= R) break;
     const OutT* s = tile + k * LD + V * lane;
     OutT* d = static_cast<OutT*>(out) + r * C + col;
+    if (!MXQ_IN_BOUNDS(r < R && col < C && r * C + col + (vec ? V : 1) <= R * C, &g_err_quant,
+                       SITE_B_DQ_COLS))
+      break;
     if (vec) {
       *reinterpret_cast<uint2*>(d) = *reinterpret_cast<const uint2*>(s);
     } else {
@@ -301,7 +310,9 @@ extern "C" mxq_status mxq_quantize_dual(const void* x, int64_t rows, int64_t col
                                         int had_c, void* codes_c, uint8_t* scales_c,
                                         void* stream) {
   if (rows % 32 != 0 || cols % 32 != 0) return MXQ_ERR_ARG;
-  if (fmt_r == MXQ_E5M2 || fmt_c == MXQ_E5M2) return MXQ_ERR_UNSUPPORTED;
+  if (fmt_r == MXQ_E5M2 || fmt_c == MXQ_E5M2)
+    return quant_launch_dual_e5m2(x, rows, cols, fmt_r, had_r, codes_r, scales_r, fmt_c, had_c,
+                                  codes_c, scales_c, stream, MXQ_SCALES_ROWMAJOR);
   return quant_launch(x, rows, cols, true, true, fmt_r, had_r != 0, codes_r, scales_r, fmt_c,
                       had_c != 0, codes_c, scales_c, stream);
 }
@@ -321,7 +332,9 @@ extern "C" mxq_status mxq_quantize_dual_ex(const void* x, int64_t rows, int64_t 
                                            int fmt_c, int had_c, void* codes_c,
                                            uint8_t* scales_c, int scale_layout, void* stream) {
   if (rows % 32 != 0 || cols % 32 != 0) return MXQ_ERR_ARG;
-  if (fmt_r == MXQ_E5M2 || fmt_c == MXQ_E5M2) return MXQ_ERR_UNSUPPORTED;
+  if (fmt_r == MXQ_E5M2 || fmt_c == MXQ_E5M2)
+    return quant_launch_dual_e5m2(x, rows, cols, fmt_r, had_r, codes_r, scales_r, fmt_c, had_c,
+                                  codes_c, scales_c, stream, scale_layout);
   return quant_launch(x, rows, cols, true, true, fmt_r, had_r != 0, codes_r, scales_r, fmt_c,
                       had_c != 0, codes_c, scales_c, stream, scale_layout);
 }

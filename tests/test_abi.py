@@ -23,6 +23,17 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) <= bound
 
 
+def test_bounds_checked_build_exports_the_same_symbols(lib):
+    # the bounds-checked variant is built from the same sources beside the
+    # library and loads on its own
+    from precision_mx_quantize_gb300 import build as _build
+    dbg = ctypes.CDLL(_build.LIB_DEBUG)
+    for n in header_symbols():
+        assert hasattr(dbg, n), n
+    dbg.mxq_status_str.restype = ctypes.c_char_p
+    assert dbg.mxq_status_str(7) == b"index out of bounds (bounds-checked build)"
+
+
 def test_version_and_status_strings(lib):
     assert lib.mxq_version() >= 1
     assert lib.mxq_status_str(0) == b"ok"
@@ -51,8 +62,9 @@ def test_argument_errors_return_before_device_work(lib):
     assert mxq.mxq_hadamard_quantize(p, -32, 64, ROW, E2, p, p, None) == 1
     assert mxq.mxq_dequantize(p, p, 64, 48, ROW, E4, p, 0, None) == 1
     assert mxq.mxq_dequantize(p, p, 64, 64, ROW, E4, p, 3, None) == 1
-    # E5M2 is a single-layout format: the dual pass rejects it
-    assert mxq.mxq_quantize_dual(p, 64, 64, mxq.E5M2, 0, p, p, E2, 1, p, p, None) == 3
+    # the dual pass takes E5M2 on either side, with the same shape rules
+    assert mxq.mxq_quantize_dual(p, 64, 40, mxq.E5M2, 0, p, p, E2, 1, p, p, None) == 1
+    assert mxq.mxq_quantize_dual(p, 64, 64, mxq.E5M2, 0, p, p, 9, 1, p, p, None) == 1
     assert mxq.mxq_quantize(p, 64, 64, ROW, 3, p, p, None) == 1
     # ablation: a sign mask needs the rotation; the usual shape rules apply
     A = mxq.mxq_quantize_ablation

@@ -67,6 +67,10 @@ def test_colwise_parity(fmt, had, shape):
     ("e4m3", False, "e4m3", False),  # weights
     ("e2m1", True, "e2m1", True),    # both axes rotated, E2M1
     ("e2m1", False, "e4m3", True),
+    ("e5m2", False, "e5m2", False),  # E5M2 on either side, with and without the rotation
+    ("e5m2", True, "e2m1", True),
+    ("e4m3", False, "e5m2", True),
+    ("e2m1", True, "e5m2", False),
 ])
 @pytest.mark.parametrize("shape", [(32, 32), (96, 160), (160, 288), (384, 256)])
 def test_dual_parity(fr, hr, fc, hc, shape):
