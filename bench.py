@@ -992,7 +992,51 @@ def config_cases(peaks):
     del d, dy, x, A, B, C
     mxq.check()
     torch.cuda.empty_cache()
+    out["f1_mxfp8_allgather_gate_up_28672x4096"] = allgather_case()
     return out
+
+
+def allgather_case(out_f=28672, in_f=4096):
+    """The MXFP8 low-precision all-gather of a weight's dim-0 shards (the
+    gate+up weight, 28672x4096): each rank quantizes its rows and the codes
+    and scales are all-gathered, against the bf16 all-gather it replaces.
+    In a world of one rank the gather is a local copy, so the figure is the
+    quantize-plus-copy cost; bytes count what each rank receives."""
+    import socket
+
+    import torch
+    import torch.distributed as dist
+
+    from precision_mx_quantize_gb300 import fsdp_gather, mxq, synth
+    created = False
+    if not dist.is_initialized():
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                                world_size=1)
+        created = True
+    try:
+        world, rank = dist.get_world_size(), dist.get_rank()
+        lo, hi = fsdp_gather.shard_bounds(out_f, world, rank)
+        shard = synth.weight(out_f, in_f, 1)[lo:hi].contiguous().cuda()
+        codes = torch.empty((out_f, in_f), dtype=torch.uint8, device="cuda")
+        scales = torch.empty((out_f, in_f // 32), dtype=torch.uint8, device="cuda")
+        full = torch.empty((out_f, in_f), dtype=torch.bfloat16, device="cuda")
+        ms_mx = _time_rotating([lambda: fsdp_gather.gather_mx_weight(shard, out=(codes, scales))])
+        ms_bf = _time_rotating([lambda: dist.all_gather_into_tensor(full, shard)])
+        mxq.check()
+        b_mx = fsdp_gather.gathered_bytes(out_f, in_f)
+        b_bf = out_f * in_f * 2
+        return {"config": f"MXFP8 all-gather of dim-0 shards, weight {out_f}x{in_f}, world {world}",
+                "ms_mxfp8": round(ms_mx, 4), "ms_bf16": round(ms_bf, 4),
+                "bytes_mxfp8": b_mx, "bytes_bf16": b_bf,
+                "volume_ratio": round(b_mx / b_bf, 4),
+                "GB/s_mxfp8": round(b_mx / ms_mx / 1e6, 1), "GB/s_bf16": round(b_bf / ms_bf / 1e6, 1),
+                "note": "world 1: the gather is a local copy; ms_mxfp8 includes quantizing the shard"}
+    finally:
+        if created:
+            dist.destroy_process_group()
 
 
 def sweep():

@@ -63,7 +63,10 @@ typedef enum {
   MXQ_ERR_UNSUPPORTED = 3,  /* valid request the library does not implement   */
   MXQ_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed               */
   MXQ_ERR_TIMEOUT = 5,      /* a device-side wait gave up (see mxq_check)      */
-  MXQ_ERR_WORKSPACE = 6     /* workspace too small                             */
+  MXQ_ERR_WORKSPACE = 6,    /* workspace too small                             */
+  MXQ_ERR_BOUNDS = 7        /* bounds-checked build only: a kernel computed an
+                               index outside the extent its arguments imply
+                               (the access was skipped; see mxq_check)       */
 } mxq_status;
 
 /* Element formats: E4M3 and E5M2 (MXFP8, one byte per element) and E2M1
@@ -138,9 +141,9 @@ mxq_status mxq_hadamard_quantize(const void* x, int64_t rows, int64_t cols, int 
  * Hadamard if had_r != 0) and the column-wise transposed output (fmt_c,
  * Hadamard if had_c != 0).  The forward/dgrad operand and the Wgrad operand
  * of the same tensor ([AMD-FP4] §02) come from a single pass.
- * Needs rows % 32 == 0, cols % 32 == 0; fmt_r, fmt_c are MXQ_E4M3 or
- * MXQ_E2M1 (MXQ_E5M2 returns MXQ_ERR_UNSUPPORTED here; use mxq_quantize).
- * Outputs as in mxq_quantize.
+ * Needs rows % 32 == 0, cols % 32 == 0; fmt_r and fmt_c are each MXQ_E4M3,
+ * MXQ_E5M2 or MXQ_E2M1 ([LUMEN] §1 names FP8 E5M2 beside E4M3), in any
+ * pairing.  Outputs as in mxq_quantize.
  */
 mxq_status mxq_quantize_dual(const void* x, int64_t rows, int64_t cols,
                              int fmt_r, int had_r, void* codes_r, uint8_t* scales_r,

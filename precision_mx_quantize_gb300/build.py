@@ -18,6 +18,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmxq.so")
+# bounds-checked variant: every kernel checks the global indices it computes
+# and records MXQ_ERR_BOUNDS instead of accessing out of range
+LIB_DEBUG = os.path.join(OUT_DIR, "libmxq_debug.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -34,41 +37,61 @@ def sources() -> list[str]:
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every csrc/*.cu for sm_103a and link _lib/libmxq.so; returns its path."""
-    nvcc = _nvcc()
-    os.makedirs(OUT_DIR, exist_ok=True)
-    obj_dir = os.path.join(OUT_DIR, "obj")
-    os.makedirs(obj_dir, exist_ok=True)
+def _compile_cmds(nvcc, obj_dir, debug_bounds, ptxas_info):
     common = [
         "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
         "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr",
     ]
+    if debug_bounds:
+        common += ["-DMXQ_DEBUG_BOUNDS"]
     if ptxas_info:
         common += ["-Xptxas", "-v"]
+    return [(src, [nvcc, *common, "-c", src, "-o",
+                   os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")])
+            for src in sources()]
 
-    def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *common, "-c", src, "-o", obj]
-        p = subprocess.run(cmd, capture_output=True, text=True)
-        if p.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{p.stderr}")
-        return obj, p.stderr
 
-    srcs = sources()
-    with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        results = list(ex.map(compile_one, srcs))
-    if verbose or ptxas_info:
-        for (_, log), src in zip(results, srcs):
-            if log.strip():
-                sys.stderr.write(f"== {os.path.basename(src)}\n{log}\n")
-    tmp = LIB + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results],
+def _link(nvcc, objs, lib):
+    tmp = lib + ".tmp"
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"link failed:\n{p.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
+
+
+def build(verbose: bool = False, ptxas_info: bool = False, debug_bounds: bool = True) -> str:
+    """Compile every csrc/*.cu for sm_103a and link _lib/libmxq.so (and, with
+    debug_bounds, the bounds-checked _lib/libmxq_debug.so from the same
+    sources, compiled in the same parallel batch); returns the main path."""
+    nvcc = _nvcc()
+    os.makedirs(OUT_DIR, exist_ok=True)
+    variants = [(LIB, os.path.join(OUT_DIR, "obj"), False)]
+    if debug_bounds:
+        variants.append((LIB_DEBUG, os.path.join(OUT_DIR, "obj_debug"), True))
+    jobs = []
+    for lib, obj_dir, dbg in variants:
+        os.makedirs(obj_dir, exist_ok=True)
+        jobs += [(lib, src, cmd) for src, cmd in _compile_cmds(nvcc, obj_dir, dbg, ptxas_info)]
+
+    def compile_one(job):
+        lib, src, cmd = job
+        p = subprocess.run(cmd, capture_output=True, text=True)
+        if p.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{p.stderr}")
+        return lib, src, cmd[-1], p.stderr
+
+    # the longest translation units first, so that they do not end last
+    jobs.sort(key=lambda j: -os.path.getsize(j[1]))
+    with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
+        results = list(ex.map(compile_one, jobs))
+    if verbose or ptxas_info:
+        for lib, src, _, log in results:
+            if log.strip() and lib == LIB:
+                sys.stderr.write(f"== {os.path.basename(src)}\n{log}\n")
+    for lib, _, _ in variants:
+        _link(nvcc, sorted(o for l, _, o, _ in results if l == lib), lib)
     return LIB
 
 

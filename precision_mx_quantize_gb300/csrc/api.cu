@@ -70,6 +70,96 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
   return fn;
 }
 
+namespace {
+
+struct TmapKey {
+  const void* base;
+  uint64_t d0, d1, stride;
+  uint32_t box0, box1;
+  int dtype, swizzle, l2, dev;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && d0 == o.d0 && d1 == o.d1 && stride == o.stride && box0 == o.box0 &&
+           box1 == o.box1 && dtype == o.dtype && swizzle == o.swizzle && l2 == o.l2 && dev == o.dev;
+  }
+};
+
+struct TmapEntry {
+  bool used;
+  TmapKey key;
+  CUtensorMap map;
+};
+
+constexpr int kTmapSlots = 512;   // direct-mapped; a collision just re-encodes
+std::mutex g_tmap_mu;
+TmapEntry g_tmap[kTmapSlots];
+
+uint64_t mix(uint64_t h, uint64_t v) {
+  h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+  return h;
+}
+
+}  // namespace
+
+CUresult tensor_map_2d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint64_t d0,
+                       uint64_t d1, uint64_t stride_bytes, uint32_t box0, uint32_t box1,
+                       CUtensorMapSwizzle swizzle, CUtensorMapL2promotion l2) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CUDA_ERROR_INVALID_CONTEXT;
+  const TmapKey k{base, d0, d1, stride_bytes, box0, box1, static_cast<int>(dtype),
+                  static_cast<int>(swizzle), static_cast<int>(l2), dev};
+  uint64_t h = reinterpret_cast<uintptr_t>(base);
+  h = mix(h, d0);
+  h = mix(h, d1);
+  h = mix(h, stride_bytes);
+  h = mix(h, (uint64_t(box0) << 32) | box1);
+  h = mix(h, (uint64_t(k.dtype) << 48) | (uint64_t(k.swizzle) << 32) | (uint64_t(k.l2) << 16) |
+                 uint64_t(dev & 0xFFFF));
+  TmapEntry& e = g_tmap[h % kTmapSlots];
+  {
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    if (e.used && e.key == k) {
+      *out = e.map;
+      return CUDA_SUCCESS;
+    }
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
+  if (!encode) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[2] = {d0, d1};
+  const cuuint64_t strides[1] = {stride_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(out, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, l2,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) {
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    e.used = true;
+    e.key = k;
+    e.map = *out;
+  }
+  return r;
+}
+
+bool ensure_dynamic_smem(const void* kernel, int bytes) {
+  struct Done {
+    const void* kernel;
+    int dev, bytes;
+  };
+  static std::mutex mu;
+  static Done done[256];
+  static int n_done = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].kernel == kernel && done[i].dev == dev && done[i].bytes >= bytes) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  if (n_done < 256) done[n_done++] = Done{kernel, dev, bytes};
+  return true;
+}
+
 }  // namespace mxq
 
 using namespace mxq;
@@ -85,6 +175,7 @@ extern "C" const char* mxq_status_str(int status) {
     case MXQ_ERR_CUDA: return "CUDA error";
     case MXQ_ERR_TIMEOUT: return "device-side wait timed out";
     case MXQ_ERR_WORKSPACE: return "workspace too small";
+    case MXQ_ERR_BOUNDS: return "index out of bounds (bounds-checked build)";
     default: return "unknown status";
   }
 }
@@ -99,8 +190,8 @@ extern "C" mxq_status mxq_check(void* stream) {
     return MXQ_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return MXQ_ERR_CUDA;
-  const uint32_t words[4] = {take_quant_error(), take_ablation_error(), take_gemm_error(),
-                             take_debug_error()};
+  const uint32_t words[5] = {take_quant_error(), take_quant_e5m2_error(), take_ablation_error(),
+                             take_gemm_error(), take_debug_error()};
   for (uint32_t w : words)
     if (w) return static_cast<mxq_status>(w & 0xFFu);
   return MXQ_OK;

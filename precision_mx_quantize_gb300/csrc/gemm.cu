@@ -333,6 +333,9 @@ MXQ_DEV void store_row_codes(const uint32_t (&v)[128], const GArgs& a, int64_t r
       sw |= sc << (8 * b);
     }
   }
+  if (!MXQ_IN_BOUNDS(row < a.M && col0 + 32 * nblk <= a.N && (!a.q_scale_tc || nblk == 4),
+                     &g_err_gemm, SITE_B_GEMM_QSCALE))
+    return;
   if (a.q_scale_tc) {
     // one word of chunk (row / 128, col0 / 128): N % 128 == 0, so nblk == 4
     uint8_t* chunk = a.q_scales + ((row >> 7) * (int64_t(a.N) >> 7) + (col0 >> 7)) * 512;
@@ -430,6 +433,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       for (int t = cid; t < n_tiles && ok; t += ncl) {
         int mp, nt;
         tile_coords(t, a, mp, nt);
+        if (!MXQ_IN_BOUNDS(mp >= 0 && mp < a.n_mp && nt >= 0 && nt < a.n_nt, &g_err_gemm,
+                           SITE_B_GEMM_TILE)) {
+          ok = false;   // the MMA lane then waits out its bounded wait
+          break;
+        }
         const int mt = G_CLUSTER * mp + static_cast<int>(rank);   // this CTA's 128-row tile
         const int srow_a = mt * a.kc_per_row;                     // first scale chunk rows
         const int srow_b0 = (2 * nt) * a.kc_per_row, srow_b1 = (2 * nt + 1) * a.kc_per_row;
@@ -549,11 +557,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       // ---------------- scale copiers (leader CTA, warps 10 and 11) -------
       // Copy each stage's scales into both CTAs' tensor memory ahead of the
       // MMA lane and signal it through sf_ready (two arrivals per stage).
-      // Separate threads, because every tcgen05 instruction occupies its
-      // issuing thread for ~70-100 cycles.  E4M3: warp 10 copies the A
-      // scales and those of B rows 0-127, warp 11 those of B rows 128-255.
-      // E2M1 (twice the chunks): warp 10 the two A chunks and the first B
-      // chunk, warp 11 the other three.
+      // Separate threads get the scales into tensor memory as soon as a
+      // stage lands, while the MMA lane is still busy with earlier stages;
+      // copies issued by the MMA lane itself, just before each stage's MMAs,
+      // measured 10-30% slower.  E4M3: warp 10 copies the A scales and those
+      // of B rows 0-127, warp 11 those of B rows 128-255.  E2M1 (twice the
+      // chunks): warp 10 the two A chunks and the first B chunk, warp 11 the
+      // other three.
       const bool first = warp == 10;
       const uint32_t st0 = smem_u32(smem);
       const bool fp4 = a.fp4 != 0;
@@ -629,7 +639,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         uint8_t* chunk = a.q_scales + ((row >> 7) * (int64_t(a.N) >> 7) + (col0 >> 7)) * 512;
         *reinterpret_cast<uint32_t*>(chunk + (row & 31) * 16 + ((row & 127) >> 5) * 4) = 0u;
       }
-      if (row < a.M && col0 < a.N) {
+      if (row < a.M && col0 < a.N &&
+          MXQ_IN_BOUNDS(mp >= 0 && mp < a.n_mp && nt >= 0 && nt < a.n_nt && row >= 0 &&
+                            col0 >= 0 && (col0 & 31) == 0,
+                        &g_err_gemm, SITE_B_GEMM_STORE)) {
         const int64_t ncols = (a.N - col0) < 128 ? (a.N - col0) : 128;
         if (a.out_q) {
           const int nblk = static_cast<int>(ncols >> 5);   // N % 32 == 0
@@ -719,6 +732,9 @@ __global__ void __launch_bounds__(256)
       }
     }
     const int64_t rt = r / 128, rr = r % 128;
+    if (!MXQ_IN_BOUNDS(r < d.rows_p && kc < kcs && kc * 4 + 3 < kbp, &g_err_gemm,
+                       SITE_B_SF_CHUNKS))
+      continue;
     uint8_t* chunk = d.out + (rt * kcs + kc) * 512;
     *reinterpret_cast<uint32_t*>(chunk + (rr % 32) * 16 + (rr / 32) * 4) = w;
   }
@@ -825,28 +841,15 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
     sf_to_chunks<<<grid, 256, 0, st>>>(sa, sb, p.kb, p.kbp);
   }
 
-  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
-  if (!encode) return MXQ_ERR_CUDA;
   CUtensorMap ta, tb;
-  const cuuint32_t estr[2] = {1, 1};
-  {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.kbytes), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.kbytes)};
-    const cuuint32_t box[2] = {G_BKB, G_BM};
-    if (encode(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(A), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MXQ_ERR_CUDA;
-  }
-  {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.kbytes), static_cast<cuuint64_t>(N)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.kbytes)};
-    const cuuint32_t box[2] = {G_BKB, G_BN_CTA};
-    if (encode(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(B), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MXQ_ERR_CUDA;
-  }
+  if (tensor_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, static_cast<uint64_t>(p.kbytes),
+                    static_cast<uint64_t>(M), static_cast<uint64_t>(p.kbytes), G_BKB, G_BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
+    return MXQ_ERR_CUDA;
+  if (tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, static_cast<uint64_t>(p.kbytes),
+                    static_cast<uint64_t>(N), static_cast<uint64_t>(p.kbytes), G_BKB, G_BN_CTA,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
+    return MXQ_ERR_CUDA;
 
   // Scale chunks as 2-D tensors of 512-byte rows (128 x uint32), one row per
   // (128-row tile, k-chunk): a stage loads n_sfa consecutive rows.  The
@@ -862,13 +865,10 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
       const int64_t rows = (lines + G_BM - 1) / G_BM * kcs;
       const void* base = tc ? static_cast<const void*>(which == 0 ? sA : sB)
                             : static_cast<const void*>(ws + (which == 0 ? 0 : p.ws_a));
-      const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
-      const cuuint64_t strides[1] = {512};
-      const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(n_sfa)};
-      if (encode(which == 0 ? &tsa : &tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
-                 const_cast<void*>(base), dims, strides, box, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      if (tensor_map_2d(which == 0 ? &tsa : &tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, base, 128,
+                        static_cast<uint64_t>(rows), 512, 128, static_cast<uint32_t>(n_sfa),
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) !=
+          CUDA_SUCCESS)
         return MXQ_ERR_CUDA;
     }
   }
@@ -940,8 +940,7 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
       a.n_tiles <= 0 || a.n_nt <= 0 || a.n_mp <= 0 || (a.out_q && !a.q_scales))
     return MXQ_ERR_ARG;
 
-  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(mx_gemm_kernel),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM) != cudaSuccess)
+  if (!ensure_dynamic_smem(reinterpret_cast<const void*>(mx_gemm_kernel), G_SMEM))
     return MXQ_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];

@@ -19,7 +19,8 @@ namespace mxq {
 // ---- error words --------------------------------------------------------
 // Each translation unit owns one device error word; bit layout:
 //   bits 0-7  : mxq_status of the first failure
-//   bits 8-15 : site id of the wait that expired
+//   bits 8-15 : site id of the wait that expired (or, in the bounds-checked
+//               build, of the check that failed)
 enum : uint32_t {
   SITE_QUANT_FULL = 1,
   SITE_QUANT_DRAIN = 2,
@@ -29,11 +30,40 @@ enum : uint32_t {
   SITE_GEMM_TMEM_EMPTY = 6,
   SITE_GEMM_DRAIN = 7,
   SITE_DEBUG = 8,
+  // bounds checks of the bounds-checked build (MXQ_DEBUG_BOUNDS)
+  SITE_B_QUANT_TILE = 16,    // quantizer tile coordinates
+  SITE_B_QUANT_TMA = 17,     // quantizer TMA coordinate alignment
+  SITE_B_QUANT_SCALE = 18,   // row-major scale stores
+  SITE_B_QUANT_SCALE_TC = 19,  // chunk-layout scale stores
+  SITE_B_DQ_ROWS = 20,       // row-wise dequantizer loads / stores
+  SITE_B_DQ_COLS = 21,       // column-wise dequantizer loads / stores
+  SITE_B_GEMM_TILE = 22,     // GEMM tile coordinates
+  SITE_B_GEMM_STORE = 23,    // GEMM epilogue stores of C / codes
+  SITE_B_GEMM_QSCALE = 24,   // GEMM epilogue stores of output scales
+  SITE_B_SF_CHUNKS = 25,     // scale re-layout stores
+  SITE_B_GEMM_TMA = 26,      // GEMM TMA coordinates
 };
 
 MXQ_DEV void record_error(uint32_t* word, uint32_t status, uint32_t site) {
   atomicCAS(word, 0u, (status & 0xFFu) | ((site & 0xFFu) << 8));
 }
+
+// ---- bounds checks ------------------------------------------------------
+// In the bounds-checked build (compiled with -DMXQ_DEBUG_BOUNDS into
+// libmxq_debug.so) every global index a kernel computes from its arguments
+// is checked, before the access, against the extent those arguments imply.
+// A failed check records MXQ_ERR_BOUNDS and the site in the translation
+// unit's error word (mxq_check reports it) and the access is skipped; no
+// check traps.  In the normal build the checks compile away.
+MXQ_DEV bool bounds_ok(bool ok, uint32_t* word, uint32_t site) {
+  if (!ok) record_error(word, MXQ_ERR_BOUNDS, site);
+  return ok;
+}
+#ifdef MXQ_DEBUG_BOUNDS
+#define MXQ_IN_BOUNDS(cond, word, site) ::mxq::bounds_ok((cond), (word), (site))
+#else
+#define MXQ_IN_BOUNDS(cond, word, site) true
+#endif
 
 // ---- shared memory / mbarrier -------------------------------------------
 MXQ_DEV uint32_t smem_u32(const void* p) {

@@ -20,8 +20,29 @@ int sm_count();
 // nullptr if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 encode_tiled();
 
+// A 2-D tiled tensor map of `base` (dims d0 inner x d1, row stride in bytes,
+// box0 x box1, element strides 1, no interleave, zero fill), encoded once per
+// distinct argument set and device and then served from a small cache: the
+// encoding depends only on these arguments, so a cached map is valid for any
+// later call that passes the same ones.  Returns CUDA_SUCCESS or the
+// encoder's error.
+CUresult tensor_map_2d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint64_t d0,
+                       uint64_t d1, uint64_t stride_bytes, uint32_t box0, uint32_t box1,
+                       CUtensorMapSwizzle swizzle, CUtensorMapL2promotion l2);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `kernel` on the
+// current device, done once per (kernel, device, size).
+bool ensure_dynamic_smem(const void* kernel, int bytes);
+
+// The one-pass quantizer when either output is E5M2 (its own translation
+// unit); arguments as mxq_quantize_dual_ex, status as the C entry points.
+mxq_status quant_launch_dual_e5m2(const void* x, int64_t R, int64_t C, int fr, int hr,
+                                  void* codes_r, uint8_t* scales_r, int fc, int hc, void* codes_c,
+                                  uint8_t* scales_c, void* stream, int scale_layout);
+
 // Read and clear the device error word of each translation unit.
 uint32_t take_quant_error();
+uint32_t take_quant_e5m2_error();
 uint32_t take_ablation_error();
 uint32_t take_gemm_error();
 

@@ -469,6 +469,9 @@ MXQ_DEV void store_scales(const uint8_t* sc_tile, uint8_t* dst, int64_t n_lines,
                           int64_t nsb, int64_t blk0, int64_t nblk_valid, int i) {
   const int64_t line = line0 + i;
   if (line >= n_lines) return;
+  if (!MXQ_IN_BOUNDS(blk0 >= 0 && blk0 + (nblk_valid < 4 ? nblk_valid : int64_t(4)) <= nsb, &g_err_quant,
+                     SITE_B_QUANT_SCALE))
+    return;
   uint8_t* d = dst + line * nsb + blk0;
   const uint32_t w = *reinterpret_cast<const uint32_t*>(sc_tile + 4 * i);
   if (nblk_valid >= 4 && (reinterpret_cast<uintptr_t>(d) & 3u) == 0) {
@@ -485,6 +488,9 @@ MXQ_DEV void store_scales(const uint8_t* sc_tile, uint8_t* dst, int64_t n_lines,
 // get zero scales, so the chunk never holds a stale or NaN byte.
 MXQ_DEV void store_scales_tc(const uint8_t* sc_tile, uint8_t* dst, int64_t n_lines, int64_t line0,
                              int64_t kcs, int64_t kc, int i) {
+  if (!MXQ_IN_BOUNDS(line0 >= 0 && line0 < n_lines && kc >= 0 && kc < kcs && i >= 0 && i < 128,
+                     &g_err_quant, SITE_B_QUANT_SCALE_TC))
+    return;
   uint8_t* chunk = dst + ((line0 >> 7) * kcs + kc) * 512;
   const uint32_t w = line0 + i < n_lines ? *reinterpret_cast<const uint32_t*>(sc_tile + 4 * i) : 0u;
   *reinterpret_cast<uint32_t*>(chunk + (i & 31) * 16 + (i >> 5) * 4) = w;
@@ -563,6 +569,8 @@ __global__ void __launch_bounds__(Q_THREADS, 2)
     tile_rc<GROUPED>(t, a, rt, ct);
     const uint32_t bar = smem_u32(&bars[s]);
     const uint32_t dst = smem_u32(smem + s * Q_TILE);
+    // x of a TMA copy must be a multiple of 16 bytes (8 bf16 elements)
+    if (!MXQ_IN_BOUNDS(((ct * Q_COLS) & 7) == 0, &g_err_quant, SITE_B_QUANT_TMA)) return;
     mbar_arrive_expect_tx(bar, Q_TILE);
     tma_load_2d(dst, &tmap, bar, ct * Q_COLS, rt * Q_ROWS);
     tma_load_2d(dst + Q_HALF, &tmap, bar, ct * Q_COLS + 64, rt * Q_ROWS);
@@ -589,30 +597,35 @@ __global__ void __launch_bounds__(Q_THREADS, 2)
     int rt, ct;
     tile_rc<GROUPED>(t, a, rt, ct);
     const int64_t R0 = int64_t(rt) * Q_ROWS, C0 = int64_t(ct) * Q_COLS;
+    // the same value in every thread: a tile outside the tensor is skipped whole
+    const bool inb = MXQ_IN_BOUNDS(rt >= 0 && ct >= 0 && R0 < a.R && C0 < a.C, &g_err_quant,
+                                   SITE_B_QUANT_TILE);
     const uint8_t* st = smem + s * Q_TILE;
-    if constexpr (ROW) row_path<FR, HR, ABL>(st, out_r, sc_r, R0, C0, a, tid);
-    if constexpr (COL) col_path<FC, HC, ABL>(st, out_c, sc_c, R0, C0, a, tid);
+    if constexpr (ROW) if (inb) row_path<FR, HR, ABL>(st, out_r, sc_r, R0, C0, a, tid);
+    if constexpr (COL) if (inb) col_path<FC, HC, ABL>(st, out_c, sc_c, R0, C0, a, tid);
     fence_async_smem();
     __syncthreads();  // staging complete; stage s fully read
     if (tid == 0) {
+      // x of a TMA store must be a multiple of 16 bytes
+      const int64_t xr = FR != MXQ_E2M1 ? C0 : C0 / 2, xc = FC != MXQ_E2M1 ? R0 : R0 / 2;
       if constexpr (ROW)
-        tma_store_2d(&tm_r, smem_u32(out_r), static_cast<int32_t>(FR != MXQ_E2M1 ? C0 : C0 / 2),
-                     static_cast<int32_t>(R0));
+        if (inb && MXQ_IN_BOUNDS((xr & 15) == 0, &g_err_quant, SITE_B_QUANT_TMA))
+          tma_store_2d(&tm_r, smem_u32(out_r), static_cast<int32_t>(xr), static_cast<int32_t>(R0));
       if constexpr (COL)
-        tma_store_2d(&tm_c, smem_u32(out_c), static_cast<int32_t>(FC != MXQ_E2M1 ? R0 : R0 / 2),
-                     static_cast<int32_t>(C0));
+        if (inb && MXQ_IN_BOUNDS((xc & 15) == 0, &g_err_quant, SITE_B_QUANT_TMA))
+          tma_store_2d(&tm_c, smem_u32(out_c), static_cast<int32_t>(xc), static_cast<int32_t>(C0));
       bulk_commit();
       const int tn = t + Q_STAGES * gridDim.x;
       if (tn < a.n_tiles) issue(tn, s);
     }
     if constexpr (ROW) {
-      if (tid < Q_ROWS) {
+      if (inb && tid < Q_ROWS) {
         if (a.sc_tc) store_scales_tc(sc_r, a.scales_r, a.R, R0, a.kcs_r, C0 >> 7, tid);
         else store_scales(sc_r, a.scales_r, a.R, R0, nsb_r, C0 >> 5, (a.C - C0 + 31) >> 5, tid);
       }
     }
     if constexpr (COL) {
-      if (tid >= Q_THREADS - Q_COLS) {
+      if (inb && tid >= Q_THREADS - Q_COLS) {
         const int i = tid - (Q_THREADS - Q_COLS);
         if (a.sc_tc) store_scales_tc(sc_c, a.scales_c, a.C, C0, a.kcs_c, R0 >> 7, i);
         else store_scales(sc_c, a.scales_c, a.C, C0, nsb_c, R0 >> 5, (a.R - R0 + 31) >> 5, i);
@@ -668,17 +681,10 @@ mxq_status quant_launch_k(QuantKernel k, const void* x, int64_t R, int64_t C, bo
     if ((row && !aligned16(scales_r)) || (col && !aligned16(scales_c))) return MXQ_ERR_ALIGN;
   }
 
-  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
-  if (!encode) return MXQ_ERR_CUDA;
   CUtensorMap map;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(C) * 2};
-  const cuuint32_t box[2] = {64, Q_ROWS};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims,
-                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult cr = tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(C),
+                              static_cast<uint64_t>(R), static_cast<uint64_t>(C) * 2, 64, Q_ROWS,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (cr != CUDA_SUCCESS) return MXQ_ERR_CUDA;
 
   // Code outputs: 2-D byte tensors written by TMA stores of 128-row tiles.
@@ -687,13 +693,11 @@ mxq_status quant_launch_k(QuantKernel k, const void* x, int64_t R, int64_t C, bo
   auto code_map = [&](CUtensorMap* m, void* base, int64_t lines, int64_t line_elems,
                       int fmt) -> CUresult {
     const int64_t lb = fmt != MXQ_E2M1 ? line_elems : line_elems / 2;
-    const cuuint64_t d[2] = {static_cast<cuuint64_t>(lb), static_cast<cuuint64_t>(lines)};
-    const cuuint64_t st[1] = {static_cast<cuuint64_t>(lb)};
-    const cuuint32_t bx[2] = {fmt != MXQ_E2M1 ? 128u : 64u, static_cast<cuuint32_t>(Q_ROWS)};
-    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, d, st, bx, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  fmt != MXQ_E2M1 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return tensor_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, static_cast<uint64_t>(lb),
+                         static_cast<uint64_t>(lines), static_cast<uint64_t>(lb),
+                         fmt != MXQ_E2M1 ? 128u : 64u, static_cast<uint32_t>(Q_ROWS),
+                         fmt != MXQ_E2M1 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE);
   };
   CUtensorMap map_r, map_c;
   memset(&map_r, 0, sizeof(map_r));
@@ -719,9 +723,7 @@ mxq_status quant_launch_k(QuantKernel k, const void* x, int64_t R, int64_t C, bo
   a.kcs_r = C / 128;
   a.kcs_c = R / 128;
 
-  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM) != cudaSuccess)
-    return MXQ_ERR_CUDA;
+  if (!ensure_dynamic_smem(reinterpret_cast<const void*>(k), Q_SMEM)) return MXQ_ERR_CUDA;
   // persistent grid (every CTA resident), launched so that it may start
   // while the previous kernel on the stream drains
   const int grid = static_cast<int>(std::min<int64_t>(a.n_tiles, int64_t(2) * sm_count()));

@@ -20,7 +20,11 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_lib", "libmxq.so")
+# MXQ_BOUNDS_CHECKED=1 selects the bounds-checked build of the same library
+# (every kernel checks the global indices it computes and reports
+# MXQ_ERR_BOUNDS through mxq_check instead of accessing out of range)
+BOUNDS_CHECKED = os.environ.get("MXQ_BOUNDS_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(_HERE, "_lib", "libmxq_debug.so" if BOUNDS_CHECKED else "libmxq.so")
 
 E4M3, E2M1, E5M2 = 0, 1, 2
 ROWWISE, COLWISE_T = 0, 1
@@ -32,7 +36,8 @@ FMTS = {"e4m3": E4M3, "e2m1": E2M1, "e5m2": E5M2, E4M3: E4M3, E2M1: E2M1, E5M2: 
 AXES = {"row": ROWWISE, "col": COLWISE_T, ROWWISE: ROWWISE, COLWISE_T: COLWISE_T}
 
 STATUS = {0: "MXQ_OK", 1: "MXQ_ERR_ARG", 2: "MXQ_ERR_ALIGN", 3: "MXQ_ERR_UNSUPPORTED",
-          4: "MXQ_ERR_CUDA", 5: "MXQ_ERR_TIMEOUT", 6: "MXQ_ERR_WORKSPACE"}
+          4: "MXQ_ERR_CUDA", 5: "MXQ_ERR_TIMEOUT", 6: "MXQ_ERR_WORKSPACE",
+          7: "MXQ_ERR_BOUNDS"}
 
 # C signatures: (name, restype, argtypes)
 _I64, _P, _I, _SZ, _U64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint64
@@ -88,7 +93,21 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(device=None) -> int:
+    """The raw handle of the current CUDA stream of `device` (default: the
+    current device).  Uses torch's raw-handle accessor when it has one, which
+    skips building a Stream object on every call."""
+    if _raw_stream is not None:
+        if device is None:
+            idx = torch.cuda.current_device()
+        elif isinstance(device, int):
+            idx = device
+        else:
+            idx = device.index if device.index is not None else torch.cuda.current_device()
+        return _raw_stream(idx)
     return torch.cuda.current_stream(device).cuda_stream
 
 

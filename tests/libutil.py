@@ -10,9 +10,10 @@ from precision_mx_quantize_gb300 import mxq
 
 
 def _stale() -> bool:
-    if not os.path.exists(mxq.LIB_PATH):
+    libs = (mxq.LIB_PATH, _build.LIB, _build.LIB_DEBUG)
+    if not all(os.path.exists(p) for p in libs):
         return True
-    built = os.path.getmtime(mxq.LIB_PATH)
+    built = min(os.path.getmtime(p) for p in libs)
     srcs = _build.sources() + [os.path.join(_build.CSRC, f) for f in os.listdir(_build.CSRC)
                                if f.endswith((".cuh", ".h"))]
     srcs += [os.path.join(_build.INCLUDE, f) for f in os.listdir(_build.INCLUDE)]

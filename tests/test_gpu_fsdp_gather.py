@@ -1,6 +1,7 @@
 """The MXFP8 all-gather of dim-0 weight shards on one GPU (a world of one
-rank over NCCL): the gathered operand equals the CUDA quantization of the
-whole weight and, fed to the forward GEMM, matches the oracle."""
+rank over NCCL): the gathered operand equals the oracle's (and the CUDA
+quantizer's) quantization of the whole weight and, fed to the forward GEMM,
+matches the oracle."""
 
 import socket
 
@@ -38,6 +39,10 @@ def test_gather_then_forward_gemm(group):
     wc, ws = mxq.mx_quantize(w, "row", "e4m3")
     mxq.check()
     assert torch.equal(codes, wc) and torch.equal(scales, ws)
+    # the gathered operand is the oracle's quantization of the whole weight
+    oc, os_ = O.mx_quantize(bf16_to_f32_np(w), "row", "e4m3")
+    np.testing.assert_array_equal(to_np(codes), oc)
+    np.testing.assert_array_equal(to_np(scales), os_)
     xc, xs = mxq.mx_quantize(x, "row", "e4m3")
     y = mxq.mx_gemm(xc, xs, codes, scales, "e4m3", 1024, 6144, 4096)
     mxq.check()
