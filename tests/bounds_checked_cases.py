@@ -117,7 +117,8 @@ def main():
     B, sB = mxq.mx_quantize(xb, "row", "e4m3", scale_layout="tc")
     mxq.mx_gemm(A, sA, B, sB, "e4m3", 256, 384, 512, scale_layout="tc")
     checked("gemm tc")
-    mxq.mx_gemm_quantize(A, sA, B, sB, "e4m3", 256, 384, 512, out_fmt="e2m1",
+    # chunk-layout output scales need N % 128 (E4M3) -- N is 384
+    mxq.mx_gemm_quantize(A, sA, B, sB, "e4m3", 256, 384, 512, out_fmt="e4m3",
                          scale_layout="tc", out_scale_layout="tc")
     checked("gemm quantize tc")
     print(json.dumps({"cases": n, "errors": errors}))
