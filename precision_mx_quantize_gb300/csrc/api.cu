@@ -74,12 +74,13 @@ namespace {
 
 struct TmapKey {
   const void* base;
-  uint64_t d0, d1, stride;
-  uint32_t box0, box1;
-  int dtype, swizzle, l2, dev;
+  uint64_t d0, d1, d2, s1, s2;
+  uint32_t box0, box1, box2;
+  int rank, dtype, swizzle, l2, dev;
   bool operator==(const TmapKey& o) const {
-    return base == o.base && d0 == o.d0 && d1 == o.d1 && stride == o.stride && box0 == o.box0 &&
-           box1 == o.box1 && dtype == o.dtype && swizzle == o.swizzle && l2 == o.l2 && dev == o.dev;
+    return base == o.base && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && s1 == o.s1 && s2 == o.s2 &&
+           box0 == o.box0 && box1 == o.box1 && box2 == o.box2 && rank == o.rank &&
+           dtype == o.dtype && swizzle == o.swizzle && l2 == o.l2 && dev == o.dev;
   }
 };
 
@@ -98,22 +99,14 @@ uint64_t mix(uint64_t h, uint64_t v) {
   return h;
 }
 
-}  // namespace
-
-CUresult tensor_map_2d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint64_t d0,
-                       uint64_t d1, uint64_t stride_bytes, uint32_t box0, uint32_t box1,
-                       CUtensorMapSwizzle swizzle, CUtensorMapL2promotion l2) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CUDA_ERROR_INVALID_CONTEXT;
-  const TmapKey k{base, d0, d1, stride_bytes, box0, box1, static_cast<int>(dtype),
-                  static_cast<int>(swizzle), static_cast<int>(l2), dev};
-  uint64_t h = reinterpret_cast<uintptr_t>(base);
-  h = mix(h, d0);
-  h = mix(h, d1);
-  h = mix(h, stride_bytes);
-  h = mix(h, (uint64_t(box0) << 32) | box1);
-  h = mix(h, (uint64_t(k.dtype) << 48) | (uint64_t(k.swizzle) << 32) | (uint64_t(k.l2) << 16) |
-                 uint64_t(dev & 0xFFFF));
+// Encodes (or serves from the cache) a tiled tensor map of rank 2 or 3.
+CUresult tensor_map_nd(CUtensorMap* out, const TmapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.base);
+  for (uint64_t v : {k.d0, k.d1, k.d2, k.s1, k.s2, (uint64_t(k.box0) << 32) | k.box1,
+                     uint64_t(k.box2), (uint64_t(k.dtype) << 48) | (uint64_t(k.swizzle) << 32) |
+                                           (uint64_t(k.l2) << 16) | uint64_t(k.rank)})
+    h = mix(h, v);
+  h = mix(h, uint64_t(k.dev));
   TmapEntry& e = g_tmap[h % kTmapSlots];
   {
     std::lock_guard<std::mutex> lock(g_tmap_mu);
@@ -124,12 +117,15 @@ CUresult tensor_map_2d(CUtensorMap* out, CUtensorMapDataType dtype, const void* 
   }
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
   if (!encode) return CUDA_ERROR_NOT_FOUND;
-  const cuuint64_t dims[2] = {d0, d1};
-  const cuuint64_t strides[1] = {stride_bytes};
-  const cuuint32_t box[2] = {box0, box1};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(out, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, l2,
+  const cuuint64_t dims[3] = {k.d0, k.d1, k.d2};
+  const cuuint64_t strides[2] = {k.s1, k.s2};
+  const cuuint32_t box[3] = {k.box0, k.box1, k.box2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(out, static_cast<CUtensorMapDataType>(k.dtype),
+                            static_cast<cuuint32_t>(k.rank), const_cast<void*>(k.base), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            static_cast<CUtensorMapSwizzle>(k.swizzle),
+                            static_cast<CUtensorMapL2promotion>(k.l2),
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r == CUDA_SUCCESS) {
     std::lock_guard<std::mutex> lock(g_tmap_mu);
@@ -138,6 +134,29 @@ CUresult tensor_map_2d(CUtensorMap* out, CUtensorMapDataType dtype, const void* 
     e.map = *out;
   }
   return r;
+}
+
+}  // namespace
+
+CUresult tensor_map_2d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint64_t d0,
+                       uint64_t d1, uint64_t stride_bytes, uint32_t box0, uint32_t box1,
+                       CUtensorMapSwizzle swizzle, CUtensorMapL2promotion l2) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CUDA_ERROR_INVALID_CONTEXT;
+  const TmapKey k{base, d0, d1, 1, stride_bytes, 0, box0, box1, 1, 2, static_cast<int>(dtype),
+                  static_cast<int>(swizzle), static_cast<int>(l2), dev};
+  return tensor_map_nd(out, k);
+}
+
+CUresult tensor_map_3d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint64_t d0,
+                       uint64_t d1, uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                       uint32_t box0, uint32_t box1, uint32_t box2, CUtensorMapSwizzle swizzle,
+                       CUtensorMapL2promotion l2) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CUDA_ERROR_INVALID_CONTEXT;
+  const TmapKey k{base, d0, d1, d2, stride1_bytes, stride2_bytes, box0, box1, box2, 3,
+                  static_cast<int>(dtype), static_cast<int>(swizzle), static_cast<int>(l2), dev};
+  return tensor_map_nd(out, k);
 }
 
 bool ensure_dynamic_smem(const void* kernel, int bytes) {

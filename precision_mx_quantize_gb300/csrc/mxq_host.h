@@ -30,6 +30,13 @@ CUresult tensor_map_2d(CUtensorMap* out, CUtensorMapDataType dtype, const void* 
                        uint64_t d1, uint64_t stride_bytes, uint32_t box0, uint32_t box1,
                        CUtensorMapSwizzle swizzle, CUtensorMapL2promotion l2);
 
+// The same for a 3-D tensor (dims d0 inner, d1, d2; strides of dims 1 and 2
+// in bytes; box box0 x box1 x box2).
+CUresult tensor_map_3d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint64_t d0,
+                       uint64_t d1, uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                       uint32_t box0, uint32_t box1, uint32_t box2, CUtensorMapSwizzle swizzle,
+                       CUtensorMapL2promotion l2);
+
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `kernel` on the
 // current device, done once per (kernel, device, size).
 bool ensure_dynamic_smem(const void* kernel, int bytes);
