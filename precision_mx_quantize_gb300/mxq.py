@@ -226,7 +226,14 @@ def _on_gpu(t):
 def _need(t, name, dtype, numel, dev=None):
     """Raise unless t is a contiguous CUDA tensor of `dtype` (None: any) with
     at least `numel` elements, on device index `dev` when given.  Cheap on
-    the success path (the binding runs it on every call)."""
+    the success path (the binding runs it on every call): one combined test,
+    and the detailed checks only to word the error."""
+    try:
+        if ((dtype is None or t.dtype is dtype) and t.numel() >= numel and t.is_contiguous()
+                and _on_gpu(t) and (dev is None or t.get_device() == dev)):
+            return
+    except AttributeError:
+        pass
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
     if dtype is not None and t.dtype is not dtype:
@@ -307,14 +314,15 @@ def mx_quantize(x: torch.Tensor, axis="row", fmt="e4m3", out=None, scale_layout=
     tensor), which mx_gemm(..., scale_layout="tc") reads in place."""
     _need_input(x)
     codes, scales = out if out is not None else _alloc_codes(x, axis, fmt, scale_layout)
-    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, scale_layout, x.get_device())
+    R, C = x.shape
+    dev = x.get_device()
+    _need_codes(codes, scales, R, C, axis, fmt, scale_layout, dev)
     if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
-        _ok(mxq_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
-                         codes.data_ptr(), scales.data_ptr(), _stream(x.device)), "mxq_quantize")
+        _ok(mxq_quantize(x.data_ptr(), R, C, AXES[axis], FMTS[fmt], codes.data_ptr(),
+                         scales.data_ptr(), _stream(dev)), "mxq_quantize")
     else:
-        _ok(mxq_quantize_ex(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt], 0,
-                            codes.data_ptr(), scales.data_ptr(), SCALES_TC, _stream(x.device)),
-            "mxq_quantize_ex")
+        _ok(mxq_quantize_ex(x.data_ptr(), R, C, AXES[axis], FMTS[fmt], 0, codes.data_ptr(),
+                            scales.data_ptr(), SCALES_TC, _stream(dev)), "mxq_quantize_ex")
     return codes, scales
 
 
@@ -323,15 +331,15 @@ def hadamard_mx_quantize(x: torch.Tensor, axis="col", fmt="e2m1", out=None,
     """Fixed 32-point Hadamard rotation of each block, then MX quantization."""
     _need_input(x)
     codes, scales = out if out is not None else _alloc_codes(x, axis, fmt, scale_layout)
-    _need_codes(codes, scales, x.shape[0], x.shape[1], axis, fmt, scale_layout, x.get_device())
+    R, C = x.shape
+    dev = x.get_device()
+    _need_codes(codes, scales, R, C, axis, fmt, scale_layout, dev)
     if SCALE_LAYOUTS[scale_layout] == SCALES_ROWMAJOR:
-        _ok(mxq_hadamard_quantize(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt],
-                                  codes.data_ptr(), scales.data_ptr(), _stream(x.device)),
-            "mxq_hadamard_quantize")
+        _ok(mxq_hadamard_quantize(x.data_ptr(), R, C, AXES[axis], FMTS[fmt], codes.data_ptr(),
+                                  scales.data_ptr(), _stream(dev)), "mxq_hadamard_quantize")
     else:
-        _ok(mxq_quantize_ex(x.data_ptr(), x.shape[0], x.shape[1], AXES[axis], FMTS[fmt], 1,
-                            codes.data_ptr(), scales.data_ptr(), SCALES_TC, _stream(x.device)),
-            "mxq_quantize_ex")
+        _ok(mxq_quantize_ex(x.data_ptr(), R, C, AXES[axis], FMTS[fmt], 1, codes.data_ptr(),
+                            scales.data_ptr(), SCALES_TC, _stream(dev)), "mxq_quantize_ex")
     return codes, scales
 
 
@@ -384,7 +392,7 @@ def mx_dequantize(codes, scales, rows, cols, axis="row", fmt="e4m3", out_dtype=t
         out = torch.empty((rows, cols), dtype=out_dtype, device=codes.device)
     _need(out, "out", out_dtype, rows * cols, dev)
     _ok(mxq_dequantize(codes.data_ptr(), scales.data_ptr(), rows, cols, AXES[axis], FMTS[fmt],
-                       out.data_ptr(), od, _stream(codes.device)), "mxq_dequantize")
+                       out.data_ptr(), od, _stream(dev)), "mxq_dequantize")
     return out
 
 
