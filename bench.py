@@ -14,6 +14,10 @@ gate+up 4096->28672, down 14336->4096).  Per layer:
   dgrad    dX = dY W           MXFP8 GEMM, bf16 out
   Wgrad    dW = (H dY)^T (H X) MXFP4 GEMM, fp32 out
 
+The Wgrad GEMMs of the four layers need nothing from one another, so the
+step issues them last, as one grouped launch (deferred weight gradients, as
+a backward pass may); forward and dgrad run per layer.
+
 Headline value: GEMM TFLOP/s of the whole step (quantizers included in the
 time).  The JSON line also carries the quantizer GB/s and the MXFP8 / MXFP4
 GEMM TFLOP/s, each against the measured GB300 peaks.
@@ -200,13 +204,20 @@ def build_device_state(plan, device):
 
 # The quantizers write their scales in the tensor cores' chunk layout and
 # the GEMMs read them in place, so each layer launches 3 dual quantizers and
-# 3 GEMMs (no scale re-layout pass, no GEMM workspace).
+# its forward and dgrad GEMMs (no scale re-layout pass, no GEMM workspace);
+# the Wgrad GEMMs of all layers depend on no other layer's result and run as
+# one grouped launch at the end of the pass (deferred weight gradients).
 SCALES = "tc"
-LAUNCHES_PER_LAYER = 3 + 3
+LAUNCHES_PER_LAYER = 3 + 2
+
+
+def launches_per_step(n_layers):
+    return LAUNCHES_PER_LAYER * n_layers + 1
 
 
 def run_layer(st, mark=None):
-    """Enqueue one layer's dual quantizers and its three GEMMs on the current stream."""
+    """Enqueue one layer's dual quantizers and its forward and dgrad GEMMs on
+    the current stream (its Wgrad GEMM runs in run_wgrad)."""
     import torch
 
     from precision_mx_quantize_gb300 import mxq
@@ -225,10 +236,21 @@ def run_layer(st, mark=None):
                 scale_layout=SCALES)
     mxq.mx_gemm(dr, sdr, wc, swc, "e4m3", T, fin, fout, torch.bfloat16, out=st["dx"],
                 scale_layout=SCALES)
-    if mark:
-        mark("f4")
-    mxq.mx_gemm(dc, sdc, xc, sxc, "e2m1", fout, fin, T, torch.float32, out=st["dw"],
-                scale_layout=SCALES)
+
+
+def run_wgrad(layers):
+    """Enqueue the Wgrad GEMMs of all layers, dW = (H dY)^T (H X) in MXFP4
+    with fp32 out, as one grouped launch."""
+    import torch
+
+    from precision_mx_quantize_gb300 import mxq
+    probs = []
+    for st in layers:
+        T, fin, fout = st["L"]["T"], st["L"]["fin"], st["L"]["fout"]
+        _, _, xc, sxc = st["xq"]
+        _, _, dc, sdc = st["dyq"]
+        probs.append((dc, sdc, xc, sxc, fout, fin, T, st["dw"]))
+    mxq.mx_gemm_grouped(probs, "e2m1", torch.float32)
 
 
 def run_step(layers, events=None):
@@ -242,6 +264,9 @@ def run_step(layers, events=None):
 
     for st in layers:
         run_layer(st, mark if events is not None else None)
+    if events is not None:
+        mark("f4")
+    run_wgrad(layers)
     if events is not None:
         mark("end")
 
@@ -397,7 +422,7 @@ def gpu_arm(args, rank, world, local_rank):
         },
         "e2e": e2e,
         "configs": configs,
-        "gpu_launches": LAUNCHES_PER_LAYER * len(plan) * args.steps,
+        "gpu_launches": launches_per_step(len(plan)) * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
@@ -470,12 +495,13 @@ def e2e_measure(args, layers, flops, device):
     down = torch.cuda.Stream(device)
     n = len(layers)
     # inputs of layer i may be overwritten once the previous step's layer i
-    # computed; dW of layer i may be overwritten once it was copied back
+    # quantized them; the dW buffers once the previous step's copies left
     done_compute = [torch.cuda.Event() for _ in range(n)]
-    done_down = [torch.cuda.Event() for _ in range(n)]
+    done_down = torch.cuda.Event()
+    wgrad_done = torch.cuda.Event()
     for i in range(n):
         done_compute[i].record(compute)
-        done_down[i].record(compute)
+    done_down.record(compute)
 
     def one():
         arrived = []
@@ -490,13 +516,16 @@ def e2e_measure(args, layers, flops, device):
                 arrived.append(ev)
         for i, st in enumerate(layers):
             compute.wait_event(arrived[i])
-            compute.wait_event(done_down[i])
             run_layer(st)
             done_compute[i].record(compute)
-            with torch.cuda.stream(down):
-                down.wait_event(done_compute[i])
-                host_out[i].copy_(st["dw"], non_blocking=True)
-                done_down[i].record(down)
+        compute.wait_event(done_down)
+        run_wgrad(layers)
+        wgrad_done.record(compute)
+        with torch.cuda.stream(down):
+            down.wait_event(wgrad_done)
+            for st, ho in zip(layers, host_out):
+                ho.copy_(st["dw"], non_blocking=True)
+            done_down.record(down)
 
     steps = max(1, min(args.steps, 10))
     one()
@@ -506,8 +535,7 @@ def e2e_measure(args, layers, flops, device):
     t0.record(compute)
     for _ in range(steps):
         one()
-    for i in range(n):
-        compute.wait_event(done_down[i])
+    compute.wait_event(done_down)
     t1.record(compute)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
@@ -515,7 +543,8 @@ def e2e_measure(args, layers, flops, device):
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "overlap": "H2D, compute and D2H on separate streams, ordered per layer by events",
+            "overlap": "H2D, compute and D2H on separate streams, ordered by events (inputs per "
+                       "layer, gradients after the step's grouped Wgrad launch)",
             "link": {"h2d_GB/s": h2d_gbs, "d2h_GB/s": d2h_gbs,
                      "h2d_bound_ms": round(h2d / (h2d_gbs * 1e6), 3),
                      "note": "one pinned copy each way, measured on this box after the e2e steps"}}

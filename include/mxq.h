@@ -269,6 +269,38 @@ mxq_status mxq_gemm_quantize_ex(const void* A, const uint8_t* sA, const void* B,
                                 int out_scale_layout, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/*
+ * One problem of mxq_gemm_grouped: C[M][N] = dec(A) dec(B)^T as in mxq_gemm,
+ * with sA, sB in the tensor cores' chunk layout (MXQ_SCALES_TC), as for
+ * mxq_gemm_ex with that layout.  out_dtype: MXQ_OUT_F32 or MXQ_OUT_BF16.
+ */
+typedef struct {
+  const void* A;
+  const uint8_t* sA;
+  const void* B;
+  const uint8_t* sB;
+  void* C;
+  int64_t M, N, K;
+  int out_dtype;
+} mxq_gemm_problem;
+
+/*
+ * Several independent GEMMs of one element format in one launch: their
+ * 256x256 tiles are numbered problem after problem and run by one persistent
+ * grid, so a problem with few tiles does not leave most clusters idle in its
+ * last wave.  [AMD-FP4] §02 runs a weight-gradient (Wgrad) GEMM per linear
+ * layer; the layers' Wgrad GEMMs depend on nothing the others compute, so a
+ * backward pass can issue them together.
+ *
+ * problems: count (1..8) problems in host memory (read during the call), each
+ * with the preconditions of mxq_gemm_ex for MXQ_SCALES_TC (K % 128 == 0 for
+ * E4M3/E5M2, % 256 for E2M1; 16-byte aligned pointers; chunk-layout scales of
+ * mxq_scales_tc_bytes(M, K) and (N, K) bytes).  Each C gets exactly what
+ * mxq_gemm_ex would write for its problem, bit for bit.  The caller owns
+ * every buffer; no workspace.  Argument errors return before any launch.
+ */
+mxq_status mxq_gemm_grouped(const mxq_gemm_problem* problems, int count, int fmt, void* stream);
+
 /* Bytes of workspace mxq_gemm needs for this problem (0 on bad arguments). */
 size_t mxq_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int fmt);
 

@@ -36,6 +36,8 @@
 // first rewritten into it by a small pre-pass kernel in the caller's
 // workspace.  The kernel is launched with programmatic stream serialization
 // and waits for the previous grid (griddepcontrol) before any global access.
+#include <string.h>
+
 #include <mutex>
 
 #include "mxq_common.cuh"
@@ -68,8 +70,12 @@ constexpr uint32_t G_SFB_COL0 = 256 + 8 * G_STAGES;  // 16 columns per stage
 static_assert(G_SFB_COL0 + 16 * G_STAGES <= G_TMEM_COLS, "tensor memory budget");
 static_assert(G_STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 
+// One GEMM problem of a launch.  Fields up to q_scale_tc may differ between
+// the problems of a grouped launch; the element format, the epilogue kind and
+// the wait limit are those of problem 0 for all.
 struct GArgs {
   int32_t M, N;
+  int32_t tile0;                // first work item of this problem in the launch
   int32_t n_mp, n_nt, n_tiles;  // 256-row pair tiles along M, 256-col tiles along N
   int32_t group;                // tiles per raster group along the grouped dimension
   int32_t group_n;              // 1: groups run along N, 0: along M
@@ -89,6 +95,19 @@ struct GArgs {
   int32_t q_scale_tc;           // output scales in the tensor cores' chunk layout
   uint32_t pace_ns;             // epilogue: pause after each 16/32-byte store (see below)
   uint64_t timeout_ns;
+};
+
+// A launch: up to G_MAX_GROUP problems of one element format and their
+// tensor maps, the work items of problem i numbered from p[i].tile0.  One
+// problem is the plain GEMM; several are independent GEMMs that run as one
+// persistent grid (e.g. the weight gradients of several layers, which no
+// layer waits for), so their tiles fill the waves together.
+constexpr int G_MAX_GROUP = 8;
+struct GGroup {
+  CUtensorMap ta[G_MAX_GROUP], tb[G_MAX_GROUP], tsa[G_MAX_GROUP], tsb[G_MAX_GROUP];
+  GArgs p[G_MAX_GROUP];
+  int32_t count;
+  int32_t n_tiles;              // work items of all problems
 };
 
 // ---- tcgen05 / cluster wrappers --------------------------------------------
@@ -368,10 +387,15 @@ MXQ_DEV void tile_coords(int t, const GArgs& a, int& mp, int& nt) {
   nt = a.group_n ? gi : oi;
 }
 
+// Problem of work item t: p advances monotonically as a role walks its
+// items in increasing order.
+MXQ_DEV int problem_of(const GGroup& g, int t, int p) {
+  while (p + 1 < g.count && t >= g.p[p + 1].tile0) ++p;
+  return p;
+}
+
 __global__ void __launch_bounds__(G_THREADS, 1)
-    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                   const GArgs a) {
+    mx_gemm_kernel(const __grid_constant__ GGroup g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -390,11 +414,14 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
+  const GArgs& a0 = g.p[0];   // format, epilogue kind and wait limit of the launch
   if (threadIdx.x == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
-    prefetch_tmap(&tmSA);
-    prefetch_tmap(&tmSB);
+    for (int i = 0; i < g.count; ++i) {
+      prefetch_tmap(&g.ta[i]);
+      prefetch_tmap(&g.tb[i]);
+      prefetch_tmap(&g.tsa[i]);
+      prefetch_tmap(&g.tsb[i]);
+    }
     for (int s = 0; s < G_STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);    // leader: one arrival, bytes of both CTAs
       mbar_init(smem_u32(&empty[s]), 1);
@@ -415,10 +442,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   griddep_launch_dependents();
   const int cid = blockIdx.x / G_CLUSTER, ncl = gridDim.x / G_CLUSTER;
   const uint32_t tmem = *tmem_base_slot;
-  const int n_tiles = a.n_tiles, nk = a.nk;
-  const uint64_t tmo = a.timeout_ns;
+  const int n_tiles = g.n_tiles;
+  const uint64_t tmo = a0.timeout_ns;
 
-  const int n_sfa = a.fp4 ? 2 : 1;            // 512-byte chunks of own-A scales per stage
+  const int n_sfa = a0.fp4 ? 2 : 1;           // 512-byte chunks of own-A scales per stage
   const uint32_t sf_bytes_a = 512u * n_sfa;   // per 128 rows
   // bytes one CTA brings into a stage; the leader's barrier counts both CTAs
   const uint32_t cta_tx = G_A_BYTES + G_B_BYTES + 3 * sf_bytes_a;
@@ -430,9 +457,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const uint32_t full0 = map_to_rank(smem_u32(&full[0]), 0);
       uint32_t s = 0, phase = 0, issued = 0;
       bool ok = true;
+      int pi = 0;
       for (int t = cid; t < n_tiles && ok; t += ncl) {
+        pi = problem_of(g, t, pi);
+        const GArgs& a = g.p[pi];
+        const int nk = a.nk;
         int mp, nt;
-        tile_coords(t, a, mp, nt);
+        tile_coords(t - a.tile0, a, mp, nt);
         if (!MXQ_IN_BOUNDS(mp >= 0 && mp < a.n_mp && nt >= 0 && nt < a.n_nt, &g_err_gemm,
                            SITE_B_GEMM_TILE)) {
           ok = false;   // the MMA lane then waits out its bounded wait
@@ -451,14 +482,15 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           const uint32_t st = smem_u32(smem + s * G_STAGE_BYTES);
           const uint32_t bar = full0 + s * 8;
           if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), G_CLUSTER * cta_tx);
-          tma_load_2d_pair(st, &tmA, bar, ks * G_BKB, mt * G_BM);
-          tma_load_2d_pair(st + G_A_BYTES, &tmB, bar, ks * G_BKB,
+          tma_load_2d_pair(st, &g.ta[pi], bar, ks * G_BKB, mt * G_BM);
+          tma_load_2d_pair(st + G_A_BYTES, &g.tb[pi], bar, ks * G_BKB,
                            nt * G_BN + static_cast<int>(rank) * G_BN_CTA);
           const int kc = ks * n_sfa;
-          tma_load_2d_pair(st + G_A_BYTES + G_B_BYTES, &tmSA, bar, 0, srow_a + kc);
-          tma_load_2d_pair(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES, &tmSB, bar, 0, srow_b0 + kc);
-          tma_load_2d_pair(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES + sf_bytes_a, &tmSB, bar, 0,
-                           srow_b1 + kc);
+          tma_load_2d_pair(st + G_A_BYTES + G_B_BYTES, &g.tsa[pi], bar, 0, srow_a + kc);
+          tma_load_2d_pair(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES, &g.tsb[pi], bar, 0,
+                           srow_b0 + kc);
+          tma_load_2d_pair(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES + sf_bytes_a, &g.tsb[pi], bar,
+                           0, srow_b1 + kc);
           ++issued;
           if (++s == G_STAGES) { s = 0; phase ^= 1; }
         }
@@ -493,21 +525,24 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       // Everything that does not change per stage is computed once: each
       // tcgen05 instruction costs the issuing thread ~100 cycles, so the
       // loop keeps nothing else on its path.
-      const uint32_t fmt_code = static_cast<uint32_t>(a.elem_code);
+      const uint32_t fmt_code = static_cast<uint32_t>(a0.elem_code);
       uint32_t idesc[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t sf_id = a.fp4 ? ((2 * j) & 3) : j;
+        const uint32_t sf_id = a0.fp4 ? ((2 * j) & 3) : j;
         idesc[j] = idesc_block_scaled(fmt_code, sf_id, sf_id);
       }
       const uint32_t st0 = smem_u32(smem);
       const uint64_t adesc_s0 = smem_desc(st0, 0, 1024, 2);
       const uint64_t bdesc_s0 = smem_desc(st0 + G_A_BYTES, 0, 1024, 2);
       constexpr uint32_t kStageDesc = G_STAGE_BYTES >> 4;   // stage stride in descriptor units
-      const bool fp4 = a.fp4 != 0;
+      const bool fp4 = a0.fp4 != 0;
       uint32_t s = 0, phase = 0, tile_i = 0;
       bool ok = true;
+      int pi = 0;
       for (int t = cid; t < n_tiles && ok; t += ncl, ++tile_i) {
+        pi = problem_of(g, t, pi);
+        const int nk = g.p[pi].nk;
         if (!mbar_try_wait_cluster(smem_u32(tmem_empty), (tile_i & 1) ^ 1) &&
             !gwait(smem_u32(tmem_empty), (tile_i & 1) ^ 1, tmo, abort_flag)) {
           if (!*abort_flag) gabort(abort_flag, SITE_GEMM_TMEM_EMPTY);
@@ -566,10 +601,16 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       // other three.
       const bool first = warp == 10;
       const uint32_t st0 = smem_u32(smem);
-      const bool fp4 = a.fp4 != 0;
+      const bool fp4 = a0.fp4 != 0;
       uint32_t s = 0, phase = 0;
-      const uint32_t n_my = n_tiles > cid ? (n_tiles - cid + ncl - 1) / ncl : 0;
-      const uint32_t total = n_my * nk;
+      uint32_t total = 0;   // K stages of this cluster's work items
+      {
+        int pi = 0;
+        for (int t = cid; t < n_tiles; t += ncl) {
+          pi = problem_of(g, t, pi);
+          total += static_cast<uint32_t>(g.p[pi].nk);
+        }
+      }
       for (uint32_t it = 0; it < total; ++it) {
         if (!mbar_try_wait_cluster(smem_u32(&full[s]), phase) &&
             !gwait(smem_u32(&full[s]), phase, tmo, abort_flag)) {
@@ -610,7 +651,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int colh = (warp - 2) >> 2;            // 0: columns 0-127, 1: 128-255
     const uint32_t empty_leader = map_to_rank(smem_u32(tmem_empty), 0);
     uint32_t tile_i = 0;
+    int pi = 0;
     for (int t = cid; t < n_tiles; t += ncl, ++tile_i) {
+      pi = problem_of(g, t, pi);
+      const GArgs& a = g.p[pi];
       if (!gwait(smem_u32(tmem_full), tile_i & 1, tmo, abort_flag)) {
         if (lane == 0 && !*abort_flag) gabort(abort_flag, SITE_GEMM_TMEM_FULL);
         break;
@@ -628,7 +672,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       if (lane == 0) mbar_arrive_cluster_relaxed(empty_leader);
 
       int mp, nt;
-      tile_coords(t, a, mp, nt);
+      tile_coords(t - a.tile0, a, mp, nt);
       const uint32_t pn = t + ncl < n_tiles ? a.pace_ns : 0u;   // last tile: no pacing
       const int64_t row = (int64_t(mp) * G_CLUSTER + rank) * G_BM + quad * 32 + lane;
       const int64_t col0 = int64_t(nt) * G_BN + colh * 128;
@@ -813,15 +857,14 @@ struct OutSpec {
   int q_scale_layout;  // mxq_scale_layout of q_scales
 };
 
-mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, int fmt,
-                       int64_t M, int64_t N, int64_t K, const OutSpec& out, void* workspace,
-                       size_t workspace_bytes, void* stream, int scale_layout) {
-  void* C = out.C;
+// The argument checks of one problem: sizes, formats, pointers, alignment,
+// workspace.  No CUDA call.
+mxq_status gemm_validate(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                         int fmt, int64_t M, int64_t N, int64_t K, const void* C,
+                         const void* workspace, size_t workspace_bytes, int scale_layout) {
   Plan p;
   if (!make_plan(M, N, K, fmt, p)) return MXQ_ERR_ARG;
   if (scale_layout != MXQ_SCALES_ROWMAJOR && scale_layout != MXQ_SCALES_TC) return MXQ_ERR_ARG;
-  // scales already in the tensor-core chunk layout: no re-layout pass and
-  // no workspace; the chunks are read in place
   const bool tc = scale_layout == MXQ_SCALES_TC;
   if (!A || !sA || !B || !sB || !C || (!tc && !workspace)) return MXQ_ERR_ARG;
   if (tc && K % (fmt == MXQ_E2M1 ? 256 : 128) != 0) return MXQ_ERR_ARG;
@@ -831,6 +874,25 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
   if (tc && (!aligned16(sA) || !aligned16(sB))) return MXQ_ERR_ALIGN;
   if (!tc && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MXQ_ERR_ALIGN;
   if (!tc && workspace_bytes < static_cast<size_t>(p.ws_a + p.ws_b)) return MXQ_ERR_WORKSPACE;
+  return MXQ_OK;
+}
+
+// Validates one problem, runs its scale re-layout pass (row-major scales),
+// and fills its launch arguments and tensor maps (tile0 left at 0).
+mxq_status gemm_prepare(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                        int fmt, int64_t M, int64_t N, int64_t K, const OutSpec& out,
+                        void* workspace, size_t workspace_bytes, void* stream, int scale_layout,
+                        GArgs& a, CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& tsa,
+                        CUtensorMap& tsb) {
+  void* C = out.C;
+  const mxq_status vs = gemm_validate(A, sA, B, sB, fmt, M, N, K, C, workspace, workspace_bytes,
+                                      scale_layout);
+  if (vs != MXQ_OK) return vs;
+  Plan p;
+  make_plan(M, N, K, fmt, p);
+  // scales already in the tensor-core chunk layout: no re-layout pass and
+  // no workspace; the chunks are read in place
+  const bool tc = scale_layout == MXQ_SCALES_TC;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -841,7 +903,6 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
     sf_to_chunks<<<grid, 256, 0, st>>>(sa, sb, p.kb, p.kbp);
   }
 
-  CUtensorMap ta, tb;
   if (tensor_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, static_cast<uint64_t>(p.kbytes),
                     static_cast<uint64_t>(M), static_cast<uint64_t>(p.kbytes), G_BKB, G_BM,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
@@ -856,7 +917,6 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
   // workspace holds chunks for the padded 256-row tiles; caller-provided
   // chunks cover only the existing 128-row tiles, and loads of the missing
   // ones read the zero fill.
-  CUtensorMap tsa, tsb;
   {
     const int n_sfa = fmt == MXQ_E2M1 ? 2 : 1;
     const int64_t kcs = p.kbp / 4;
@@ -873,7 +933,7 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
     }
   }
 
-  GArgs a{};
+  a = GArgs{};
   a.M = static_cast<int32_t>(M);
   a.N = static_cast<int32_t>(N);
   a.n_mp = static_cast<int32_t>(p.mp / (G_CLUSTER * G_BM));
@@ -940,6 +1000,19 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
       a.n_tiles <= 0 || a.n_nt <= 0 || a.n_mp <= 0 || (a.out_q && !a.q_scales))
     return MXQ_ERR_ARG;
 
+  return MXQ_OK;
+}
+
+// Launches the prepared problems g.p[0..count) as one persistent grid.
+mxq_status gemm_run(GGroup& g, void* stream) {
+  int32_t tiles = 0;
+  for (int i = 0; i < g.count; ++i) {
+    if (int64_t(tiles) + g.p[i].n_tiles >= (int64_t(1) << 31)) return MXQ_ERR_ARG;
+    g.p[i].tile0 = tiles;
+    tiles += g.p[i].n_tiles;
+  }
+  g.n_tiles = tiles;
+  if (g.count < 1 || g.count > G_MAX_GROUP || tiles <= 0) return MXQ_ERR_ARG;
   if (!ensure_dynamic_smem(reinterpret_cast<const void*>(mx_gemm_kernel), G_SMEM))
     return MXQ_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -950,7 +1023,7 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(G_THREADS, 1, 1);
   cfg.dynamicSmemBytes = G_SMEM;
-  cfg.stream = st;
+  cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int max_clusters = max_gemm_clusters(cfg);
@@ -960,9 +1033,22 @@ mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const ui
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;
   if (max_clusters <= 0) return MXQ_ERR_CUDA;
-  cfg.gridDim = dim3(static_cast<unsigned>(G_CLUSTER * std::min(a.n_tiles, max_clusters)), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, mx_gemm_kernel, ta, tb, tsa, tsb, a) != cudaSuccess) return MXQ_ERR_CUDA;
+  cfg.gridDim = dim3(static_cast<unsigned>(G_CLUSTER * std::min(tiles, max_clusters)), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, mx_gemm_kernel, g) != cudaSuccess) return MXQ_ERR_CUDA;
   return launch_status();
+}
+
+mxq_status gemm_launch(const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, int fmt,
+                       int64_t M, int64_t N, int64_t K, const OutSpec& out, void* workspace,
+                       size_t workspace_bytes, void* stream, int scale_layout) {
+  GGroup g;
+  memset(&g, 0, sizeof(g));
+  const mxq_status st = gemm_prepare(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes,
+                                     stream, scale_layout, g.p[0], g.ta[0], g.tb[0], g.tsa[0],
+                                     g.tsb[0]);
+  if (st != MXQ_OK) return st;
+  g.count = 1;
+  return gemm_run(g, stream);
 }
 
 }  // namespace
@@ -1027,6 +1113,34 @@ extern "C" mxq_status mxq_gemm_quantize_ex(const void* A, const uint8_t* sA, con
   const OutSpec out{out_codes, 2, out_fmt, out_scales, out_scale_layout};
   return gemm_launch(A, sA, B, sB, fmt, M, N, K, out, workspace, workspace_bytes, stream,
                      scale_layout);
+}
+
+extern "C" mxq_status mxq_gemm_grouped(const mxq_gemm_problem* problems, int count, int fmt,
+                                       void* stream) {
+  if (!problems || count < 1 || count > G_MAX_GROUP) return MXQ_ERR_ARG;
+  // every problem is checked before any of them is prepared
+  for (int i = 0; i < count; ++i) {
+    const mxq_gemm_problem& q = problems[i];
+    if (q.out_dtype != MXQ_OUT_F32 && q.out_dtype != MXQ_OUT_BF16) return MXQ_ERR_ARG;
+    Plan p;
+    if (!make_plan(q.M, q.N, q.K, fmt, p)) return MXQ_ERR_ARG;
+    if (q.N % (q.out_dtype == MXQ_OUT_F32 ? 4 : 8) != 0) return MXQ_ERR_ALIGN;
+    const mxq_status vs = gemm_validate(q.A, q.sA, q.B, q.sB, fmt, q.M, q.N, q.K, q.C, nullptr, 0,
+                                        MXQ_SCALES_TC);
+    if (vs != MXQ_OK) return vs;
+  }
+  GGroup g;
+  memset(&g, 0, sizeof(g));
+  for (int i = 0; i < count; ++i) {
+    const mxq_gemm_problem& q = problems[i];
+    const OutSpec out{q.C, q.out_dtype == MXQ_OUT_BF16 ? 1 : 0, 0, nullptr, MXQ_SCALES_ROWMAJOR};
+    const mxq_status st = gemm_prepare(q.A, q.sA, q.B, q.sB, fmt, q.M, q.N, q.K, out, nullptr, 0,
+                                       stream, MXQ_SCALES_TC, g.p[i], g.ta[i], g.tb[i], g.tsa[i],
+                                       g.tsb[i]);
+    if (st != MXQ_OK) return st;
+  }
+  g.count = count;
+  return gemm_run(g, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -59,10 +59,18 @@ SIGNATURES = [
                                   _P]),
     ("mxq_gemm_workspace_size", _SZ, [_I64, _I64, _I64, _I]),
     ("mxq_gemm_noalloc", _I, [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P]),
+    ("mxq_gemm_grouped", _I, [_P, _I, _I, _P]),
     ("mxq_check", _I, [_P]),
     ("mxq_set_wait_timeout_ns", None, [_U64]),
     ("mxq_debug_expire_wait", _I, [_U64, _P]),
 ]
+
+class GemmProblem(ctypes.Structure):
+    """mxq_gemm_problem of the C header (field order and types as declared)."""
+    _fields_ = [("A", ctypes.c_void_p), ("sA", ctypes.c_void_p), ("B", ctypes.c_void_p),
+                ("sB", ctypes.c_void_p), ("C", ctypes.c_void_p), ("M", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("out_dtype", ctypes.c_int)]
+
 
 _lib = None
 _lock = threading.Lock()
@@ -186,6 +194,11 @@ def mxq_gemm_quantize_ex(A, sA, B, sB, fmt, M, N, K, scale_layout, out_fmt, code
 def mxq_gemm_noalloc(A, sA, B, sB, fmt, M, N, K, C, out_dtype, stream):
     """mxq_gemm with the library's fixed internal scratch (for callers that cannot allocate)."""
     return lib().mxq_gemm_noalloc(A, sA, B, sB, fmt, M, N, K, C, out_dtype, stream)
+
+
+def mxq_gemm_grouped(problems, count, fmt, stream):
+    """problems: address of `count` GemmProblem structures in host memory."""
+    return lib().mxq_gemm_grouped(problems, count, fmt, stream)
 
 
 def mxq_gemm_workspace_size(M, N, K, fmt):
@@ -423,6 +436,36 @@ def mx_gemm(A, sA, B, sB, fmt, M, N, K, out_dtype=torch.float32, out=None, works
                  out.data_ptr(), od, workspace.data_ptr(), workspace.numel(),
                  _stream(A.device)), "mxq_gemm")
     return out
+
+
+def mx_gemm_grouped(problems, fmt, out_dtype=torch.float32):
+    """Independent GEMMs of one format in one launch (see mxq_gemm_grouped).
+
+    problems: list of (A, sA, B, sB, M, N, K) or (A, sA, B, sB, M, N, K, out),
+    with the scales in the tensor cores' chunk layout (as returned by the
+    quantizers with scale_layout="tc").  Returns the list of outputs C, each
+    bitwise what mx_gemm(..., scale_layout="tc") would return."""
+    if not 1 <= len(problems) <= 8:
+        raise ValueError("mx_gemm_grouped takes 1 to 8 problems")
+    od = _out_code(out_dtype)
+    arr = (GemmProblem * len(problems))()
+    outs = []
+    dev = None
+    for i, pr in enumerate(problems):
+        A, sA, B, sB, M, N, K = pr[:7]
+        d = _need_operands(A, sA, B, sB, fmt, M, N, K, "tc")
+        if dev is None:
+            dev = d
+        elif d != dev:
+            raise ValueError(f"problem {i} is on device {d}, problem 0 on {dev}")
+        out = pr[7] if len(pr) > 7 else torch.empty((M, N), dtype=out_dtype, device=A.device)
+        _need(out, f"out[{i}]", out_dtype, M * N, dev)
+        arr[i] = GemmProblem(A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(),
+                             out.data_ptr(), M, N, K, od)
+        outs.append(out)
+    _ok(mxq_gemm_grouped(ctypes.addressof(arr), len(problems), FMTS[fmt], _stream(dev)),
+        "mxq_gemm_grouped")
+    return outs
 
 
 def mx_gemm_quantize(A, sA, B, sB, fmt, M, N, K, out_fmt="e4m3", out=None, workspace=None,

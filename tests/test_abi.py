@@ -110,3 +110,47 @@ def test_binding_signatures_match_the_header():
                 assert arg in (ctypes.c_void_p, ctypes.c_char_p), (name, i, decl)
             else:
                 assert arg is want, (name, i, decl, arg)
+
+
+def test_gemm_problem_struct_matches_the_header(tmp_path):
+    # the binding's ctypes mirror of mxq_gemm_problem has the C layout: a C
+    # program compiled against the header prints sizeof and every offset
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    import os
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    src = tmp_path / "layout.c"
+    fields = [f for f, _ in mxq.GemmProblem._fields_]
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"mxq.h\"\nint main(void) {\n"
+                   "  printf(\"%zu\", sizeof(mxq_gemm_problem));\n" +
+                   "".join(f"  printf(\" %zu\", offsetof(mxq_gemm_problem, {f}));\n" for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    cuda_inc = "/usr/local/cuda/include"
+    subprocess.run([cc, "-I", inc, "-I", cuda_inc, str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [ctypes.sizeof(mxq.GemmProblem)] + [getattr(mxq.GemmProblem, f).offset for f in fields]
+    assert got == want
+
+
+def test_gemm_grouped_argument_errors(lib):
+    p = ctypes.c_void_p(16 * 1024)
+    arr = (mxq.GemmProblem * 9)()
+    for i in range(9):
+        arr[i] = mxq.GemmProblem(p.value, p.value, p.value, p.value, p.value, 256, 256, 256, 0)
+    addr = ctypes.addressof(arr)
+    assert mxq.mxq_gemm_grouped(None, 1, mxq.E4M3, None) == 1
+    assert mxq.mxq_gemm_grouped(addr, 0, mxq.E4M3, None) == 1
+    assert mxq.mxq_gemm_grouped(addr, 9, mxq.E4M3, None) == 1
+    arr[1].K = 96                      # K % 32 == 0 but not % 128 (chunk-layout scales)
+    assert mxq.mxq_gemm_grouped(addr, 2, mxq.E4M3, None) == 1
+    arr[1].K = 256
+    arr[1].out_dtype = 5
+    assert mxq.mxq_gemm_grouped(addr, 2, mxq.E4M3, None) == 1
+    arr[1].out_dtype = 0
+    arr[1].N = 258                     # fp32 rows must stay 16-byte aligned
+    assert mxq.mxq_gemm_grouped(addr, 2, mxq.E4M3, None) == 2
