@@ -13,9 +13,12 @@
 // CTA streams 128x128 bf16 tiles into a 2-stage shared-memory ring with TMA
 // (128-byte swizzle, two 64-column boxes per tile); all 8 warps read the tile
 // from shared memory:
-//   row path: a thread owns the same 32-column block of rows r and r+64,
-//             so both blocks travel through the packed fp32x2 ALU together;
+//   row path: a thread owns the same 32-column block of rows r and r+64;
 //   col path: a thread owns the same 32-row block of two adjacent columns.
+// Unrotated blocks (and the ablation variants) travel through the packed
+// fp32x2 ALU side by side, one block per lane of each pair; rotated blocks
+// go one after the other with adjacent elements paired, the first
+// butterfly stage taken straight from the bf16 inputs.
 // Each block is (optionally) rotated in registers, its amax reduced, its
 // E8M0 exponent taken from the amax bits, and its elements converted with
 // the hardware's round-to-nearest-even saturating E4M3/E2M1 conversions.
@@ -147,6 +150,40 @@ MXQ_DEV void fwht32_pair(float2 (&v)[32]) {
   }
 }
 
+// One 32-block in v[16] with v[i] = (x[2i], x[2i+1]) and stage h = 1 already
+// applied: stages h = 2, 4, 8, 16 on packed pairs of adjacent elements (for
+// h >= 2 elements 2i and 2i + 1 have the same partner offset).
+MXQ_DEV void fwht32_single_from2(float2 (&v)[16]) {
+#pragma unroll
+  for (int hh = 1; hh < 16; hh <<= 1) {  // hh = h / 2, in pairs
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & hh) == 0) {
+        const float2 a = v[i], b = v[i + hh];
+        v[i] = add2(a, b);
+        v[i + hh] = sub2(a, b);
+      }
+    }
+  }
+}
+
+// First butterfly stage straight from bf16 inputs with the mixed-precision
+// add: for a the bf16 in the low (bfly_lo) or high (bfly_hi) half of w and
+// c an fp32, s = RN(a + c) and d = RN(a - c) -- the same values as widening
+// a first (widening is exact), one integer op fewer per pair.
+MXQ_DEV void bfly_lo(uint32_t w, float c, float& s, float& d) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, l, %3;\n\t}"
+      : "=f"(s), "=f"(d)
+      : "r"(w), "f"(c));
+}
+MXQ_DEV void bfly_hi(uint32_t w, float c, float& s, float& d) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, h, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+      : "=f"(s), "=f"(d)
+      : "r"(w), "f"(c));
+}
+
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
 // easy as 1, 2, 3", SC 2011): ten rounds, each two 32x32 -> 64-bit products
 // whose halves are xored with the other two words and the round key, the key
@@ -231,10 +268,12 @@ MXQ_DEV float sr_round(float v, uint32_t r) {
 // output.  Its block amax is RN(max|a| * c) (rounding is monotone), and
 // RN(a * c) * 2^(127-s) equals RN(a * (c * 2^(127-s))) whenever the result
 // is a normal fp32; below that both are far under half the smallest element
-// step and encode as a zero of the same sign.  So one multiply by the exact
-// constant c * 2^(127-s) replaces two, except when that constant would be
-// subnormal (s > 250, only for blocks whose amax is above 2^125), where the
-// two multiplies are kept.
+// step and encode as a zero of the same sign.  So one multiply by the
+// constant c * 2^(127-s) replaces two.  That constant is exact: a finite
+// butterfly output is below 2^128, so the rotated amax is below 2^125.5 and
+// s <= 252 - emax <= 250 for every element format, which keeps
+// c * 2^(127-s) >= 2^-125.5 a normal fp32 (a NaN or infinite amax gives
+// s = 255, whose codes are discarded).
 //
 // With ABL_SR the scaled elements are rounded stochastically before the
 // conversion; rnd(g, ra, rb) supplies the random words of elements 4g..4g+3
@@ -260,17 +299,9 @@ MXQ_DEV void quant_pair(float2 (&v)[32], uint32_t abA, uint32_t abB,
     abB = __float_as_uint(__fmul_rn(mB, c)) & 0x7FFFFFFFu;
     sA = scale_of(abA, Elem<FMT>::emax);
     sB = scale_of(abB, Elem<FMT>::emax);
-    const uint32_t sa = sA == 255u ? 0u : sA, sb = sB == 255u ? 0u : sB;
-    if (max(sa, sb) > 250u) {
-      const float2 c2 = make_float2(c, c);
-      const float2 m2 = make_float2(inv_scale(sA), inv_scale(sB));
+    const float2 m2 = make_float2(__fmul_rn(c, inv_scale(sA)), __fmul_rn(c, inv_scale(sB)));
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = mul2(mul2(v[j], c2), m2);
-    } else {
-      const float2 m2 = make_float2(__fmul_rn(c, inv_scale(sA)), __fmul_rn(c, inv_scale(sB)));
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], m2);
-    }
+    for (int j = 0; j < 32; ++j) v[j] = mul2(v[j], m2);
   } else {
     sA = scale_of(abA, Elem<FMT>::emax);
     sB = scale_of(abB, Elem<FMT>::emax);
@@ -322,6 +353,50 @@ MXQ_DEV void quant_pair(float2 (&v)[32], uint32_t abA, uint32_t abB,
   }
 }
 
+// Rotate (stage 1 already applied), scale and encode one 32-block held as
+// v[16] = (x[2i], x[2i+1]) pairs: the same arithmetic as quant_pair's
+// rotated path for one block.  Processing the two blocks of a thread one
+// after the other, rather than packed lane-wise, leaves the scheduler two
+// independent instruction streams and saves the widening of stage-1 inputs
+// (measured: dual Hadamard E2M1 16384 x 8192 from 0.62 to 0.66 of the copy
+// rate, bit-identical outputs).
+template <int FMT>
+MXQ_DEV void quant_single_had(float2 (&v)[16], uint32_t (&o)[Elem<FMT>::words], uint32_t& sc) {
+  fwht32_single_from2(v);
+  float t[6];
+#pragma unroll
+  for (int i = 0; i < 5; ++i)
+    t[i] = max3_abs_nan(max3_abs_nan(v[3 * i].x, v[3 * i].y, v[3 * i + 1].x), v[3 * i + 1].y,
+                        max3_abs_nan(v[3 * i + 2].x, v[3 * i + 2].y, v[3 * i + 2].y));
+  t[5] = max3_abs_nan(v[15].x, v[15].y, v[15].y);
+  const float m =
+      max3_abs_nan(max3_abs_nan(t[0], t[1], t[2]), max3_abs_nan(t[3], t[4], t[5]), t[5]);
+  const float c = hadamard_c();
+  sc = scale_of(__float_as_uint(__fmul_rn(m, c)) & 0x7FFFFFFFu, Elem<FMT>::emax);
+  const float k = __fmul_rn(c, inv_scale(sc));  // exact: s <= 250 (see quant_pair)
+  const float2 m2 = make_float2(k, k);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = mul2(v[i], m2);
+  if constexpr (FMT == MXQ_E4M3) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      o[k] = cvt_e4m3x4(v[2 * k].x, v[2 * k].y, v[2 * k + 1].x, v[2 * k + 1].y);
+  } else if constexpr (FMT == MXQ_E5M2) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      o[k] = cvt_e5m2x4(v[2 * k].x, v[2 * k].y, v[2 * k + 1].x, v[2 * k + 1].y);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      o[k] = cvt_e2m1x8(v[4 * k].x, v[4 * k].y, v[4 * k + 1].x, v[4 * k + 1].y, v[4 * k + 2].x,
+                        v[4 * k + 2].y, v[4 * k + 3].x, v[4 * k + 3].y);
+  }
+  if (sc == 255u) {
+#pragma unroll
+    for (int k = 0; k < Elem<FMT>::words; ++k) o[k] = 0u;
+  }
+}
+
 // Byte offset of (row r, byte b of its 128-byte row) in a 128B-swizzled tile.
 MXQ_DEV int swz128(int r, int b) { return r * 128 + ((((b >> 4) ^ (r & 7)) << 4) | (b & 15)); }
 // Byte offset of (row r, byte b of its 64-byte row) in a 64B-swizzled tile.
@@ -354,6 +429,27 @@ MXQ_DEV void row_path(const uint8_t* st, uint8_t* out_tile, uint8_t* sc_tile, in
     const uint4 B = *reinterpret_cast<const uint4*>(half + (r + 64) * 128 + off);
     wa[4 * i] = A.x; wa[4 * i + 1] = A.y; wa[4 * i + 2] = A.z; wa[4 * i + 3] = A.w;
     wb[4 * i] = B.x; wb[4 * i + 1] = B.y; wb[4 * i + 2] = B.z; wb[4 * i + 3] = B.w;
+  }
+  if constexpr (HAD && ABL == 0) {
+    // stage 1 pairs elements 2k (low half) and 2k + 1 (high half) of word k
+    uint32_t oA[Elem<FMT>::words], oB[Elem<FMT>::words], sA, sB;
+    {
+      float2 v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) bfly_lo(wa[k], bf16hi(wa[k]), v[k].x, v[k].y);
+      quant_single_had<FMT>(v, oA, sA);
+    }
+    {
+      float2 v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) bfly_lo(wb[k], bf16hi(wb[k]), v[k].x, v[k].y);
+      quant_single_had<FMT>(v, oB, sB);
+    }
+    stage_block<FMT>(out_tile, r, q, oA);
+    stage_block<FMT>(out_tile, r + 64, q, oB);
+    sc_tile[r * 4 + q] = static_cast<uint8_t>(sA);
+    sc_tile[(r + 64) * 4 + q] = static_cast<uint8_t>(sB);
+    return;
   }
   if constexpr ((ABL & ABL_SIGN) != 0) {
 #pragma unroll
@@ -414,6 +510,28 @@ MXQ_DEV void col_path(const uint8_t* st, uint8_t* out_tile, uint8_t* sc_tile, in
   uint32_t w[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) w[j] = *reinterpret_cast<const uint32_t*>(half + swz128(32 * b + j, pb));
+  if constexpr (HAD && ABL == 0) {
+    // stage 1 pairs rows j and j + 1 of each column (column A in the low
+    // halves, column B in the high halves)
+    uint32_t oA[Elem<FMT>::words], oB[Elem<FMT>::words], sA, sB;
+    {
+      float2 v[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) bfly_lo(w[j], bf16lo(w[j + 1]), v[j / 2].x, v[j / 2].y);
+      quant_single_had<FMT>(v, oA, sA);
+    }
+    {
+      float2 v[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) bfly_hi(w[j], bf16hi(w[j + 1]), v[j / 2].x, v[j / 2].y);
+      quant_single_had<FMT>(v, oB, sB);
+    }
+    stage_block<FMT>(out_tile, 2 * cp, b, oA);
+    stage_block<FMT>(out_tile, 2 * cp + 1, b, oB);
+    sc_tile[(2 * cp) * 4 + b] = static_cast<uint8_t>(sA);
+    sc_tile[(2 * cp + 1) * 4 + b] = static_cast<uint8_t>(sB);
+    return;
+  }
   if constexpr ((ABL & ABL_SIGN) != 0) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) w[j] ^= ((a.sign_mask >> j) & 1u) * 0x80008000u;
