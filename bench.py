@@ -960,13 +960,24 @@ def config_cases(peaks):
     y = torch.empty((256, 1024), dtype=torch.float32, device="cuda")
     q1 = lambda: mxq.mx_quantize(x, "row", "e4m3", out=(c, sc))
     d1 = lambda: mxq.mx_dequantize(c, sc, 256, 1024, "row", "e4m3", out=y)
+    # the C-ABI entry points called directly (pointers taken once): the
+    # library's own per-call host cost, without the binding's tensor checks
+    L, st = mxq.lib(), mxq._stream(x.device)
+    xp, cp, sp, yp = x.data_ptr(), c.data_ptr(), sc.data_ptr(), y.data_ptr()
+    q1_abi = lambda: L.mxq_quantize(xp, 256, 1024, mxq.ROWWISE, mxq.FMTS["e4m3"], cp, sp, st)
+    d1_abi = lambda: L.mxq_dequantize(cp, sp, 256, 1024, mxq.ROWWISE, mxq.FMTS["e4m3"], yp,
+                                      mxq.OUT_F32, st)
     out["cfg1_round_trip_256x1024_e4m3"] = {
         "config": "round trip 256x1024 E4M3",
         "quantize_us": round(_time_rotating([q1], reps=200) * 1e3, 2),
         "dequantize_us": round(_time_rotating([d1], reps=200) * 1e3, 2),
+        "quantize_us_abi": round(_time_rotating([q1_abi], reps=200) * 1e3, 2),
+        "dequantize_us_abi": round(_time_rotating([d1_abi], reps=200) * 1e3, 2),
         "quantize_us_graph": round(_time_rotating([q1], reps=200, graph=True) * 1e3, 2),
         "dequantize_us_graph": round(_time_rotating([d1], reps=200, graph=True) * 1e3, 2),
-        "timing": "us per call launched one by one from Python; _graph: the same calls in a CUDA graph"}
+        "timing": "us per call launched one by one from Python through the tensor binding; "
+                  "_abi: the C entry points called directly through ctypes with the pointers "
+                  "taken once; _graph: the binding's calls in a CUDA graph"}
     del x, c, sc, y
 
     x = synth.hadamard_dual_activation()["x"].cuda()
