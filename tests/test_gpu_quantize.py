@@ -131,6 +131,40 @@ def test_special_values(fmt, had):
     _check(x, "col", fmt, had)
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+def test_largest_finite_rotated_blocks(fmt):
+    """Blocks whose rotated amax is the largest finite one (a single input at
+    the bf16 maximum, scale byte 125 - emax + 127) and blocks whose butterfly
+    sums overflow (two such inputs: scale 255, zero codes), in both layouts
+    and the one-pass kernel, against the oracle."""
+    bmax = np.frombuffer(np.uint32(0x7F7F0000).tobytes(), np.float32)[0]
+    x = np.random.default_rng(9).standard_normal((128, 128)).astype(np.float32)
+    x[0, :32] = 0.0
+    x[0, 7] = bmax                   # row block 0 of row 0
+    x[1, 32:64] = 0.0
+    x[1, 40] = -bmax                 # row block 1 of row 1
+    x[2, 64:96] = 0.0
+    x[2, 70] = bmax
+    x[2, 90] = bmax                  # an overflowing row block
+    x[32:64, 100] = 0.0
+    x[40, 100] = -bmax               # column block 1 of column 100
+    x[64:96, 101] = 0.0
+    x[64, 101] = bmax
+    x[95, 101] = bmax                # an overflowing column block
+    xb = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    _check(xb, "row", fmt, True)
+    _check(xb, "col", fmt, True)
+    xn = bf16_to_f32_np(xb)
+    cr, sr, cc, sc = mxq.mx_quantize_dual(xb, fmt, True, fmt, True)
+    mxq.check()
+    for (codes, scales), axis in (((cr, sr), "row"), ((cc, sc), "col")):
+        ec, es = O.hadamard_mx_quantize(xn, axis, fmt)
+        np.testing.assert_array_equal(to_np(scales), es)
+        np.testing.assert_array_equal(to_np(codes), ec)
+    emax = {"e4m3": 8, "e2m1": 2, "e5m2": 15}[fmt]
+    assert int(to_np(sr)[0, 0]) == 125 - emax + 127 and int(to_np(sr)[2, 2]) == 255
+
+
 @pytest.mark.parametrize("case", load_blocks(), ids=lambda c: c["name"])
 def test_hand_derived_blocks_on_gpu(case):
     x = torch.tensor(case["x"], dtype=torch.float32).to(torch.bfloat16).reshape(1, 32).cuda()

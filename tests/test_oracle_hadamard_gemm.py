@@ -124,6 +124,31 @@ def test_hadamard_quantize_is_rotate_then_quantize():
     assert np.array_equal(c0, c1) and np.array_equal(s0, s1)
 
 
+def test_largest_finite_rotated_block_reaches_the_scale_bound():
+    """The largest finite bf16 alone in a block gives the largest finite
+    rotated amax: every butterfly output is +-x, and RN(x * c) < 2^125.5, so
+    the scale byte is 125 - emax + 127 (250 for E2M1), the upper bound the
+    kernels' single multiplier c * 2^(127-s) relies on.  Two such inputs
+    overflow a butterfly sum: scale 255 and zero codes."""
+    bmax = np.frombuffer(np.uint32(0x7F7F0000).tobytes(), np.float32)[0]
+    x = np.zeros((2, 32), np.float32)
+    x[0, 5] = bmax
+    x[1, 3] = -bmax
+    for fmt, emax in ((O.E2M1, 2), (O.E4M3, 8), (O.E5M2, 15)):
+        codes, s = O.hadamard_mx_quantize(x, "row", fmt)
+        assert s[0, 0] == 125 - emax + 127 and s[1, 0] == s[0, 0]
+        vals = O.mx_dequantize(codes, s, fmt)
+        # every rotated value is +-RN(|x| * c); scaled by 2^(127 - s) it is
+        # 1.9921875 * 2^(emax + 0.5), which each format rounds onto its grid
+        y = np.float32(np.float64(bmax) * np.float64(O.fwht_scale()))
+        q = O.round_to_element(np.float64(y) / 2.0 ** (125 - emax), fmt)
+        assert np.all(np.abs(vals) == np.float32(abs(float(q)) * 2.0 ** (125 - emax)))
+    y = x.copy()
+    y[0, 9] = bmax
+    codes, s = O.hadamard_mx_quantize(y[:1], "row", O.E2M1)
+    assert s[0, 0] == 255 and not np.any(codes)
+
+
 def _int_codes(rng, fmt, shape, lim):
     """Codes whose element values are small integers in [-lim, lim]."""
     table = O.decode_table(fmt)
