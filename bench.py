@@ -1111,7 +1111,8 @@ def sweep():
               "cfg4_mlp_wgrad_mxfp4_14336x4096x16384": _oracle_gemm_rates(
                   M=14336, N=4096, K=16384, fmt="e2m1")}
     for k, d in config_cases(peaks).items():
-        d["cpu_oracle"] = dict(host, **orates[k])
+        if k in orates:   # the all-gather case has no oracle leg (it moves bytes, computes nothing new)
+            d["cpu_oracle"] = dict(host, **orates[k])
         emit(d)
     torch.cuda.empty_cache()
 

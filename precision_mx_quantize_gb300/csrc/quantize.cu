@@ -240,6 +240,234 @@ __global__ void __launch_bounds__(256) mx_dequant_cols(const uint8_t* __restrict
   }
 }
 
+// Column-wise codes [C][R] back to out [R][C] through TMA, for outputs whose
+// rows are 16-byte multiples (C % 8 bf16, C % 4 fp32).  The mirror of the
+// quantizer's column path: a persistent grid of 2 CTAs per SM streams code
+// tiles (TC lines x 128 rows, 128- or 64-byte swizzle) into a 2-stage ring;
+// each thread decodes the same 32-row block of two adjacent columns (bf16:
+// packed pairs, one 4-byte shared store per row) or of one column (fp32)
+// into a 128-row output tile held as two 128-byte-wide halves with the
+// 128-byte swizzle; one TMA store per half writes it, double-buffered so
+// the stores drain while the next tile is decoded.  TMA clips the edges:
+// code lines and rows past the tensor read zeros, and nothing is stored
+// past it.
+constexpr int DQT_THREADS = 256;
+constexpr int DQT_TR = 128;                 // output rows per tile (4 blocks)
+constexpr int DQT_HALF = DQT_TR * 128;      // one 128-byte-wide half of the output tile
+constexpr int DQT_OUT = 2 * DQT_HALF;       // output tile: 128 rows x 256 bytes
+constexpr int DQT_STAGES = 2;
+
+template <int FMT, bool BF16>
+struct DqtShape {
+  static constexpr int TC = BF16 ? 128 : 64;           // output columns (code lines) per tile
+  static constexpr int LB = FMT == MXQ_E2M1 ? 64 : 128;  // code bytes per line and tile
+  static constexpr int CODE = TC * LB;                 // code tile bytes
+  static constexpr int OFF_OUT = DQT_STAGES * CODE;     // a multiple of 1024
+  static constexpr int OFF_BAR = OFF_OUT + 2 * DQT_OUT;
+  static constexpr int SMEM = OFF_BAR + 64 + 1024;
+};
+
+struct DqtArgs {
+  int64_t R, C;
+  int32_t n_ct, n_tiles;
+  const uint8_t* scales;
+  uint64_t timeout_ns;
+};
+
+// Byte address of code byte k of line L in a swizzled code tile.
+template <int FMT>
+MXQ_DEV int dqt_code_off(int L, int k) {
+  if constexpr (FMT != MXQ_E2M1) return swz128(L, k);
+  else return swz64(L, k);
+}
+
+// The 32 elements of block b (rows 32b.. of the tile) of code line L, times
+// `scale` (the same products as the row-wise and column-wise kernels).
+template <int FMT>
+MXQ_DEV void dqt_decode32(const uint8_t* code, int L, int b, float scale, float (&f)[32]) {
+  if constexpr (FMT != MXQ_E2M1) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 w = *reinterpret_cast<const uint4*>(code + dqt_code_off<FMT>(L, 32 * b + 16 * h));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 lo = FMT == MXQ_E4M3 ? e4m3x2_to_f32(ws[i] & 0xFFFFu) : e5m2x2_to_f32(ws[i] & 0xFFFFu);
+        const float2 hi = FMT == MXQ_E4M3 ? e4m3x2_to_f32(ws[i] >> 16) : e5m2x2_to_f32(ws[i] >> 16);
+        f[16 * h + 4 * i] = lo.x * scale;
+        f[16 * h + 4 * i + 1] = lo.y * scale;
+        f[16 * h + 4 * i + 2] = hi.x * scale;
+        f[16 * h + 4 * i + 3] = hi.y * scale;
+      }
+    }
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(code + dqt_code_off<FMT>(L, 16 * b));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int bidx = 0; bidx < 4; ++bidx) {
+        const float2 q = e2m1x2_to_f32((ws[i] >> (8 * bidx)) & 0xFFu);
+        f[8 * i + 2 * bidx] = q.x * scale;
+        f[8 * i + 2 * bidx + 1] = q.y * scale;
+      }
+    }
+  }
+}
+
+template <int FMT, bool BF16>
+MXQ_DEV void dqt_tile(const uint8_t* code, uint8_t* ot, int64_t r0, int64_t c0, const DqtArgs& a,
+                      int tid) {
+  using S = DqtShape<FMT, BF16>;
+  const int b = tid >> 6;                     // row block of the tile (warp-uniform)
+  if (r0 + 32 * b >= a.R) return;             // rows past the tensor are not stored
+  const int64_t nsb = a.R >> 5, rb = (r0 >> 5) + b;
+  if constexpr (BF16) {
+    const int p = tid & 63;                   // column pair 2p, 2p + 1 of the tile
+    const int64_t c = c0 + 2 * p;             // C % 8 == 0: both columns or neither
+    if (c >= a.C) return;
+    if (!MXQ_IN_BOUNDS(c + 1 < a.C && rb < nsb, &g_err_quant, SITE_B_DQ_COLS)) return;
+    float fa[32], fb[32];
+    dqt_decode32<FMT>(code, 2 * p, b, scale_value(a.scales[c * nsb + rb]), fa);
+    dqt_decode32<FMT>(code, 2 * p + 1, b, scale_value(a.scales[(c + 1) * nsb + rb]), fb);
+    uint8_t* half = ot + (p >> 5) * DQT_HALF;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const __nv_bfloat162 v = __floats2bfloat162_rn(fa[j], fb[j]);
+      *reinterpret_cast<__nv_bfloat162*>(half + swz128(32 * b + j, 4 * (p & 31))) = v;
+    }
+  } else {
+    const int cl = tid & 63;                  // one column of the tile
+    const int64_t c = c0 + cl;
+    if (c >= a.C) return;
+    if (!MXQ_IN_BOUNDS(rb < nsb, &g_err_quant, SITE_B_DQ_COLS)) return;
+    float f[32];
+    dqt_decode32<FMT>(code, cl, b, scale_value(a.scales[c * nsb + rb]), f);
+    uint8_t* half = ot + (cl >> 5) * DQT_HALF;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      *reinterpret_cast<float*>(half + swz128(32 * b + j, 4 * (cl & 31))) = f[j];
+  }
+}
+
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(DQT_THREADS, 2)
+    mx_dequant_cols_tma(const __grid_constant__ CUtensorMap tm_codes,
+                        const __grid_constant__ CUtensorMap tm_out, const DqtArgs a) {
+  using S = DqtShape<FMT, BF16>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    prefetch_tmap(&tm_codes);
+    prefetch_tmap(&tm_out);
+#pragma unroll
+    for (int s = 0; s < DQT_STAGES; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int t, int s) {
+    const int rt = t / a.n_ct, ct = t - rt * a.n_ct;
+    const int32_t x = rt * S::LB;             // code bytes: 128 rows of one-byte or half-byte codes
+    if (!MXQ_IN_BOUNDS((x & 15) == 0, &g_err_quant, SITE_B_DQ_COLS)) return;
+    const uint32_t bar = smem_u32(&bars[s]);
+    mbar_arrive_expect_tx(bar, S::CODE);
+    tma_load_2d(smem_u32(smem + s * S::CODE), &tm_codes, bar, x, ct * S::TC);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < DQT_STAGES; ++s) {
+      const int t = blockIdx.x + s * gridDim.x;
+      if (t < a.n_tiles) issue(t, s);
+    }
+  }
+  int it = 0;
+  bool failed = false;
+  for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
+    const int s = it % DQT_STAGES;
+    const bool ok = mbar_wait(smem_u32(&bars[s]), (it / DQT_STAGES) & 1, a.timeout_ns);
+    // the stores of two tiles ago (the same output buffer) have read it
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    if (!__syncthreads_and(ok)) {
+      failed = true;
+      break;
+    }
+    const int rt = t / a.n_ct, ct = t - rt * a.n_ct;
+    const int64_t r0 = int64_t(rt) * DQT_TR, c0 = int64_t(ct) * S::TC;
+    uint8_t* ot = smem + S::OFF_OUT + (it & 1) * DQT_OUT;
+    const bool inb = MXQ_IN_BOUNDS(r0 < a.R && c0 < a.C, &g_err_quant, SITE_B_DQ_COLS);
+    if (inb) dqt_tile<FMT, BF16>(smem + s * S::CODE, ot, r0, c0, a, tid);
+    fence_async_smem();
+    __syncthreads();                          // output tile complete; stage s fully read
+    if (tid == 0) {
+      if (inb) {
+        tma_store_2d(&tm_out, smem_u32(ot), static_cast<int32_t>(c0), static_cast<int32_t>(r0));
+        if (c0 + S::TC / 2 < a.C)
+          tma_store_2d(&tm_out, smem_u32(ot + DQT_HALF), static_cast<int32_t>(c0 + S::TC / 2),
+                       static_cast<int32_t>(r0));
+      }
+      bulk_commit();
+      const int tn = t + DQT_STAGES * gridDim.x;
+      if (tn < a.n_tiles) issue(tn, s);
+    }
+  }
+  if (tid == 0) bulk_wait0();
+  if (failed && tid == 0) {
+    record_error(&g_err_quant, MXQ_ERR_TIMEOUT, SITE_QUANT_FULL);
+    for (int k = it; k < it + DQT_STAGES; ++k) {
+      const int t = blockIdx.x + k * gridDim.x;
+      if (t >= a.n_tiles) break;
+      if (!mbar_wait(smem_u32(&bars[k % DQT_STAGES]), (k / DQT_STAGES) & 1, a.timeout_ns))
+        record_error(&g_err_quant, MXQ_ERR_TIMEOUT, SITE_QUANT_DRAIN);
+    }
+  }
+}
+
+// Encodes the two tensor maps and launches the TMA column-wise dequantizer;
+// false when the shape or buffers do not suit it (the caller then uses
+// mx_dequant_cols), MXQ status through `st` otherwise.
+template <int FMT, bool BF16>
+bool dequant_cols_tma(const uint8_t* codes, const uint8_t* scales, int64_t R, int64_t C,
+                      void* out, cudaStream_t stream, mxq_status& st) {
+  using S = DqtShape<FMT, BF16>;
+  const int esz = BF16 ? 2 : 4;
+  if ((C * esz) % 16 != 0 || R >= (int64_t(1) << 31) || C >= (int64_t(1) << 31)) return false;
+  const int64_t line = FMT != MXQ_E2M1 ? R : R / 2;    // code bytes per column
+  CUtensorMap tc, to;
+  if (tensor_map_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, static_cast<uint64_t>(line),
+                    static_cast<uint64_t>(C), static_cast<uint64_t>(line), S::LB, S::TC,
+                    FMT != MXQ_E2M1 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS ||
+      tensor_map_2d(&to, BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    out, static_cast<uint64_t>(C), static_cast<uint64_t>(R),
+                    static_cast<uint64_t>(C) * esz, S::TC / 2, DQT_TR, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE) != CUDA_SUCCESS) {
+    st = MXQ_ERR_CUDA;
+    return true;
+  }
+  DqtArgs a;
+  memset(&a, 0, sizeof(a));
+  a.R = R;
+  a.C = C;
+  a.n_ct = static_cast<int32_t>((C + S::TC - 1) / S::TC);
+  const int64_t n_rt = (R + DQT_TR - 1) / DQT_TR;
+  if (n_rt * a.n_ct >= (int64_t(1) << 31)) return false;
+  a.n_tiles = static_cast<int32_t>(n_rt * a.n_ct);
+  a.scales = scales;
+  a.timeout_ns = wait_timeout_ns();
+  auto k = mx_dequant_cols_tma<FMT, BF16>;
+  if (!ensure_dynamic_smem(reinterpret_cast<const void*>(k), S::SMEM)) {
+    st = MXQ_ERR_CUDA;
+    return true;
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(a.n_tiles, int64_t(2) * sm_count()));
+  k<<<grid, DQT_THREADS, S::SMEM, stream>>>(tc, to, a);
+  st = launch_status();
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -377,6 +605,20 @@ extern "C" mxq_status mxq_dequantize(const void* codes, const uint8_t* scales, i
 #undef MXQ_DQ_ROWS
   } else {
     if (rows % 32 != 0) return MXQ_ERR_ARG;
+    mxq_status tst = MXQ_OK;
+    bool done;
+    if (fmt == MXQ_E4M3) {
+      done = bf ? dequant_cols_tma<MXQ_E4M3, true>(c8, scales, rows, cols, out, st, tst)
+                : dequant_cols_tma<MXQ_E4M3, false>(c8, scales, rows, cols, out, st, tst);
+    } else if (fmt == MXQ_E5M2) {
+      done = bf ? dequant_cols_tma<MXQ_E5M2, true>(c8, scales, rows, cols, out, st, tst)
+                : dequant_cols_tma<MXQ_E5M2, false>(c8, scales, rows, cols, out, st, tst);
+    } else {
+      done = bf ? dequant_cols_tma<MXQ_E2M1, true>(c8, scales, rows, cols, out, st, tst)
+                : dequant_cols_tma<MXQ_E2M1, false>(c8, scales, rows, cols, out, st, tst);
+    }
+    if (done) return tst;
+    // output rows that are not 16-byte multiples: the shared-memory transpose
     const int tr = 64, tc = bf ? DqColsTile<0, true>::TC : DqColsTile<0, false>::TC;
     const int64_t n_cb = (cols + tc - 1) / tc, n_rb = (rows + tr - 1) / tr;
     if (n_cb * n_rb >= (int64_t(1) << 31)) return MXQ_ERR_ARG;
