@@ -256,11 +256,13 @@ def test_dequantize_arbitrary_scales():
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("shape", [(32, 1), (64, 37), (96, 130), (160, 258), (4128, 1001)])
+@pytest.mark.parametrize("shape", [(32, 1), (64, 37), (96, 130), (160, 258), (4128, 1001),
+                                   (32, 8), (160, 264), (288, 136), (4128, 1000)])
 def test_dequantize_colwise_ragged(fmt, out_dtype, shape):
     # column-wise codes [cols][rows] of random bytes and random scales: odd
-    # and ragged column counts (scalar tail stores), partial row and column
-    # tiles
+    # and ragged column counts (the shared-memory transpose with scalar tail
+    # stores), and column counts whose output rows are 16-byte multiples (the
+    # TMA path) with partial row and column tiles
     R, C = shape
     g = torch.Generator().manual_seed(R * 7 + C)
     cb = R // 2 if fmt == "e2m1" else R
