@@ -86,3 +86,23 @@ def test_grouped_block_wgrad_shapes_match_single_calls():
     mxq.check()
     for got, ref in zip(outs, singles):
         assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("n_problems", [1, 8])
+def test_grouped_limits_match_single_calls(n_problems):
+    # the group of one (the single-problem path) and the largest group (8
+    # problems of mixed shapes: single tiles, ragged M and N, K from one to
+    # five 128-element chunks), MXFP8 with bf16 output
+    shapes = [(128, 128, 128), (256, 384, 256), (200, 264, 384), (512, 128, 640),
+              (128, 520, 128), (384, 256, 512), (136, 392, 256), (256, 1024, 128)][:n_problems]
+    probs, singles = [], []
+    for i, (M, N, K) in enumerate(shapes):
+        _, _, A, sA, B, sB = _operands(M, N, K, "e4m3", 70 + 3 * i, False)
+        probs.append((A, sA, B, sB, M, N, K))
+        singles.append(mxq.mx_gemm(A, sA, B, sB, "e4m3", M, N, K, torch.bfloat16,
+                                   scale_layout="tc"))
+    outs = mxq.mx_gemm_grouped(probs, "e4m3", torch.bfloat16)
+    mxq.check()
+    assert len(outs) == n_problems
+    for (M, N, K), got, ref in zip(shapes, outs, singles):
+        assert torch.equal(got, ref), (M, N, K)
